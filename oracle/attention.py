@@ -1,0 +1,318 @@
+"""Plain fp64 CPU oracle for softmax attention: forward, first backward and
+backward-over-backward (BoB).
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import, call or
+execute this module: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline / reference arm of ``bench.py`` use it.  It shares no code with the
+CUDA library (no kernels, headers, helpers or constants).
+
+Sources (all four web pages describe one paper, "FlashBoB: I/O-Efficient
+Exact Backward-over-Backward for Softmax Attention"):
+
+* abstract (aiqbench.com news item and arxivdaily.com): attention forward and
+  first backward in the FlashAttention sense; BoB differentiates through the
+  first backward;
+* evolve.pub review, "Scope & Claims": BoB is J_g^T applied to upstream
+  matrices at (dQ, dK, dV) (paper section 4.1);
+* evolve.pub review, FAQ "What is backward-over-backward (BoB)": the
+  Jacobian-transpose-vector product of the first-backward map;
+* evolve.pub review, FAQ "Is FlashBoB an approximation?": the outputs are
+  exact, so the oracle is the plain definition;
+* evolve.pub review, Strengths ("Genuinely new algorithmic insight"): the
+  paper's Appendix C derives every identity node by node with reverse-mode
+  chain rule.  The pages do not print those equations; ``bob_rows`` below is
+  that reverse-mode sweep written out for the graph of g, in the order of the
+  graph's nodes.
+
+Notation (per head, row-major, rows i = queries, rows j = keys):
+    S = tau Q K^T,  P = softmax_row(S),  O = P V,  L_i = logsumexp_j S_ij
+    g(Q, K, V, dO) = (dQ, dK, dV) with
+        dV = P^T dO,  dP = dO V^T,  D = rowsum(dO o O),
+        dS = P o (dP - D 1^T),  dQ = tau dS K,  dK = tau dS^T Q
+    BoB(UQ, UK, UV) = gradient of f = <UQ,dQ> + <UK,dK> + <UV,dV>
+        with respect to (Q, K, V, dO)  ->  (gQ, gK, gV, gdO)
+        (the pages write these four outputs as ed(Q), ed(K), ed(V), ed(dO)).
+
+Readings where the pages are silent (each is also listed in the design doc):
+* g is a function of (Q, K, V, dO) only; O is not an independent input, so
+  D = rowsum(dO o O) is differentiated through O = P V.
+* tau multiplies the scores once: S = tau Q K^T.
+* L is the natural-log row logsumexp.
+* Non-causal attention.
+
+Every row of every intermediate (S, P, O, dP, D, dS) depends only on the
+query rows of Q and dO of that row, so the graph of g splits exactly into
+independent query-row blocks: the query-row outputs (dQ, gQ, gdO, D, L, O)
+of a block are complete, and the key-side outputs (dK, dV, gK, gV) are sums
+of per-block contributions.  ``_row_blocks`` uses that to bound memory for
+long sequences; the arithmetic inside a block is the unblocked definition.
+
+Parity pins (tests/test_oracle_*.py): library softmax/logsumexp, brute force
+loops, torch.autograd fp64 first and double backward, a sympy symbolic double
+derivative, central finite differences through the adjoint identity, the
+closed-form reduction of the evolve.pub review's Strengths item "Theory
+honestly scoped" (paper Lemma E.2) and invariants.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "attn_fwd_head",
+    "attn_bwd_rows",
+    "bob_rows",
+    "row_scalars",
+    "attn_fwd",
+    "attn_bwd",
+    "attn_bob",
+    "bob_row_scalars",
+]
+
+# Largest number of fp64 score elements one row block materialises
+# (a block of r rows holds several r x N matrices).
+_BLOCK_ELEMS = 1 << 23
+
+
+def _f64(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64)
+
+
+def _softmax_rows(S: np.ndarray):
+    """Row softmax and natural-log logsumexp with the usual max shift."""
+    m = S.max(axis=1, keepdims=True)
+    e = np.exp(S - m)
+    s = e.sum(axis=1, keepdims=True)
+    P = e / s
+    L = (m + np.log(s))[:, 0]
+    return P, L
+
+
+# ---------------------------------------------------------------------------
+# forward (abstract: FlashAttention-style forward; here materialised)
+# ---------------------------------------------------------------------------
+
+def attn_fwd_head(Q, K, V, tau):
+    """O = softmax(tau Q K^T) V and L = logsumexp rows, one head, fp64."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    S = tau * (Q @ K.T)
+    P, L = _softmax_rows(S)
+    O = P @ V
+    return O, L
+
+
+# ---------------------------------------------------------------------------
+# first backward g (abstract; evolve.pub FAQ "What is backward-over-backward")
+# ---------------------------------------------------------------------------
+
+def attn_bwd_rows(Qr, K, V, dOr, tau):
+    """First backward restricted to the query rows Qr, dOr of one head.
+
+    Returns (dQ_rows, dK_part, dV_part, D_rows): the row outputs are complete,
+    the key-side outputs are this block's contribution to the sums over rows.
+    """
+    Qr, K, V, dOr = _f64(Qr), _f64(K), _f64(V), _f64(dOr)
+    S = tau * (Qr @ K.T)
+    P, _ = _softmax_rows(S)
+    O = P @ V
+    dV = P.T @ dOr
+    dP = dOr @ V.T
+    D = (dOr * O).sum(axis=1)
+    dS = P * (dP - D[:, None])
+    dQ = tau * (dS @ K)
+    dK = tau * (dS.T @ Qr)
+    return dQ, dK, dV, D
+
+
+# ---------------------------------------------------------------------------
+# backward over backward: reverse mode through the graph of g, node by node
+# (evolve.pub review, "Scope & Claims" and Strengths; paper section 4.1 and
+# Appendix C)
+# ---------------------------------------------------------------------------
+
+def bob_rows(Qr, K, V, dOr, UQr, UK, UV, tau):
+    """Reverse-mode sweep of f = <UQ,dQ> + <UK,dK> + <UV,dV> for one query-row
+    block of one head.
+
+    Returns (gQ_rows, gK_part, gV_part, gdO_rows).  Every node of the first
+    backward is materialised; adjoints are named ``<node>_bar``.
+    """
+    Qr, K, V, dOr = _f64(Qr), _f64(K), _f64(V), _f64(dOr)
+    UQr, UK, UV = _f64(UQr), _f64(UK), _f64(UV)
+
+    # ---- forward sweep: the nodes of g ---------------------------------
+    S = tau * (Qr @ K.T)                      # S = tau Q K^T
+    P, _ = _softmax_rows(S)                   # P = softmax_row(S)
+    O = P @ V                                 # O = P V
+    dP = dOr @ V.T                            # dP = dO V^T
+    D = (dOr * O).sum(axis=1)                 # D = rowsum(dO o O)
+    dS = P * (dP - D[:, None])                # dS = P o (dP - D 1^T)
+    # outputs: dQ = tau dS K, dK = tau dS^T Q, dV = P^T dO
+
+    # ---- reverse sweep ---------------------------------------------------
+    Q_bar = np.zeros_like(Qr)
+    K_bar = np.zeros_like(K)
+    V_bar = np.zeros_like(V)
+    dO_bar = np.zeros_like(dOr)
+    P_bar = np.zeros_like(P)
+
+    # output seeds: dQ_bar = UQ, dK_bar = UK, dV_bar = UV
+    # dQ = tau dS K
+    dS_bar = tau * (UQr @ K.T)
+    K_bar += tau * (dS.T @ UQr)
+    # dK = tau dS^T Q
+    dS_bar += tau * (Qr @ UK.T)
+    Q_bar += tau * (dS @ UK)
+    # dV = P^T dO
+    P_bar += dOr @ UV.T
+    dO_bar += P @ UV
+    # dS = P o (dP - D 1^T)
+    P_bar += dS_bar * (dP - D[:, None])
+    dP_bar = dS_bar * P
+    D_bar = -(dS_bar * P).sum(axis=1)
+    # D = rowsum(dO o O)
+    dO_bar += D_bar[:, None] * O
+    O_bar = D_bar[:, None] * dOr
+    # dP = dO V^T
+    dO_bar += dP_bar @ V
+    V_bar += dP_bar.T @ dOr
+    # O = P V
+    P_bar += O_bar @ V.T
+    V_bar += P.T @ O_bar
+    # P = softmax_row(S)
+    S_bar = P * (P_bar - (P * P_bar).sum(axis=1, keepdims=True))
+    # S = tau Q K^T
+    Q_bar += tau * (S_bar @ K)
+    K_bar += tau * (S_bar.T @ Qr)
+
+    return Q_bar, K_bar, V_bar, dO_bar
+
+
+def row_scalars(Qr, K, V, dOr, UQr, UK, UV, tau):
+    """The two row scalars of the hierarchical affine structure for a row block.
+
+    The pages name them alpha and E (evolve.pub review, Summary and Key claims:
+    paper Prop. 4.1) without printing formulas.  Reading used here, with
+    B = tau (UQ K^T + Q UK^T) the adjoint reaching dS, C = dO UV^T the adjoint
+    reaching P through dV, and dP = dO V^T:
+
+        alpha_i = sum_j P_ij B_ij
+        E_i     = sum_j P_ij (C_ij + B_ij dP_ij)
+
+    so that -alpha is the adjoint of D and E - 2 D alpha is the row centre
+    rowsum(P o P_bar) of the softmax reverse step in ``bob_rows``.
+    """
+    Qr, K, V, dOr = _f64(Qr), _f64(K), _f64(V), _f64(dOr)
+    UQr, UK, UV = _f64(UQr), _f64(UK), _f64(UV)
+    S = tau * (Qr @ K.T)
+    P, _ = _softmax_rows(S)
+    dP = dOr @ V.T
+    B = tau * (UQr @ K.T + Qr @ UK.T)
+    C = dOr @ UV.T
+    alpha = (P * B).sum(axis=1)
+    E = (P * (C + B * dP)).sum(axis=1)
+    return alpha, E
+
+
+# ---------------------------------------------------------------------------
+# batched drivers over [..., N, d] arrays
+# ---------------------------------------------------------------------------
+
+def _row_blocks(N: int):
+    r = max(1, min(N, _BLOCK_ELEMS // max(N, 1)))
+    for s in range(0, N, r):
+        yield slice(s, min(N, s + r))
+
+
+def _heads(x):
+    x = _f64(x)
+    lead = x.shape[:-2]
+    return x.reshape((-1,) + x.shape[-2:]), lead
+
+
+def attn_fwd(Q, K, V, tau):
+    """O [..., N, d], L [..., N] for every head of [..., N, d] inputs."""
+    Qh, lead = _heads(Q)
+    Kh, _ = _heads(K)
+    Vh, _ = _heads(V)
+    O = np.empty(Qh.shape[:-1] + (Vh.shape[-1],))
+    L = np.empty(Qh.shape[:-1])
+    for h in range(Qh.shape[0]):
+        for rows in _row_blocks(Qh.shape[1]):
+            O[h, rows], L[h, rows] = attn_fwd_head(Qh[h, rows], Kh[h], Vh[h], tau)
+    return O.reshape(lead + O.shape[1:]), L.reshape(lead + L.shape[1:])
+
+
+def attn_bwd(Q, K, V, dO, tau):
+    """(dQ, dK, dV, D) for every head of [..., N, d] inputs."""
+    Qh, lead = _heads(Q)
+    Kh, _ = _heads(K)
+    Vh, _ = _heads(V)
+    dOh, _ = _heads(dO)
+    dQ = np.empty_like(Qh)
+    dK = np.zeros_like(Kh)
+    dV = np.zeros_like(Vh)
+    D = np.empty(Qh.shape[:-1])
+    for h in range(Qh.shape[0]):
+        for rows in _row_blocks(Qh.shape[1]):
+            q, k, v, dd = attn_bwd_rows(Qh[h, rows], Kh[h], Vh[h], dOh[h, rows], tau)
+            dQ[h, rows] = q
+            dK[h] += k
+            dV[h] += v
+            D[h, rows] = dd
+    shp = lambda a: a.reshape(lead + a.shape[1:])
+    return shp(dQ), shp(dK), shp(dV), shp(D)
+
+
+def attn_bob(Q, K, V, dO, UQ, UK, UV, tau):
+    """(gQ, gK, gV, gdO) for every head of [..., N, d] inputs."""
+    Qh, lead = _heads(Q)
+    Kh, _ = _heads(K)
+    Vh, _ = _heads(V)
+    dOh, _ = _heads(dO)
+    UQh, _ = _heads(UQ)
+    UKh, _ = _heads(UK)
+    UVh, _ = _heads(UV)
+    gQ = np.empty_like(Qh)
+    gK = np.zeros_like(Kh)
+    gV = np.zeros_like(Vh)
+    gdO = np.empty_like(dOh)
+    for h in range(Qh.shape[0]):
+        for rows in _row_blocks(Qh.shape[1]):
+            q, k, v, o = bob_rows(Qh[h, rows], Kh[h], Vh[h], dOh[h, rows],
+                                  UQh[h, rows], UKh[h], UVh[h], tau)
+            gQ[h, rows] = q
+            gK[h] += k
+            gV[h] += v
+            gdO[h, rows] = o
+    shp = lambda a: a.reshape(lead + a.shape[1:])
+    return shp(gQ), shp(gK), shp(gV), shp(gdO)
+
+
+def bob_row_scalars(Q, K, V, dO, UQ, UK, UV, tau):
+    """(alpha, E) [..., N] for every head (see ``row_scalars``)."""
+    Qh, lead = _heads(Q)
+    Kh, _ = _heads(K)
+    Vh, _ = _heads(V)
+    dOh, _ = _heads(dO)
+    UQh, _ = _heads(UQ)
+    UKh, _ = _heads(UK)
+    UVh, _ = _heads(UV)
+    alpha = np.empty(Qh.shape[:-1])
+    E = np.empty(Qh.shape[:-1])
+    for h in range(Qh.shape[0]):
+        for rows in _row_blocks(Qh.shape[1]):
+            alpha[h, rows], E[h, rows] = row_scalars(
+                Qh[h, rows], Kh[h], Vh[h], dOh[h, rows], UQh[h, rows], UKh[h], UVh[h], tau)
+    return alpha.reshape(lead + alpha.shape[1:]), E.reshape(lead + E.shape[1:])
+
+
+def bob_sampled_rows(Q, K, V, dO, UQ, UK, UV, tau, rows):
+    """Query-row outputs (gQ, gdO) of one head restricted to the given rows.
+
+    The row-side outputs of a row are complete from that row alone (see the
+    module docstring), so long sequences can be checked on a sample of rows.
+    """
+    rows = np.asarray(rows)
+    gQ, _, _, gdO = bob_rows(_f64(Q)[rows], K, V, _f64(dO)[rows], _f64(UQ)[rows], UK, UV, tau)
+    return gQ, gdO
