@@ -65,6 +65,11 @@ WORKLOADS = {
     "peaky_b4h32_n8192_d128":
         Workload("peaky_b4h32_n8192_d128", 4, 32, 8192, 128, "bf16", 1.0 / math.sqrt(128),
                  (4.0, 4.0, 1.0, 1.0, 1.0, 1.0, 1.0)),
+    # profiler case: the wide-head shape with 8 heads (inputs 235 MB > L2)
+    "wide_head_b2h4_n16384_d128":
+        Workload("wide_head_b2h4_n16384_d128", 2, 4, 16384, 128, "bf16", 1.0 / math.sqrt(128)),
+    "long_context_b1h8_n16384_d64":
+        Workload("long_context_b1h8_n16384_d64", 1, 8, 16384, 64, "bf16", 1.0 / 8.0),
     # closed-form reduction, fp32
     "closed_form_fp32_b1h1_n32768_d128":
         Workload("closed_form_fp32_b1h1_n32768_d128", 1, 1, 32768, 128, "fp32",

@@ -146,11 +146,7 @@ def run_ours(args, w):
         torch.cuda.synchronize()
 
     def max_over_ranks(v):
-        if ws == 1:
-            return v
-        t = torch.tensor([v], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(v, ws, dev)
 
     for _ in range(args.warmup):
         step()
@@ -210,9 +206,9 @@ def run_ours(args, w):
     flops_step = (FLOPS_FWD + FLOPS_BWD + FLOPS_BOB) * unit
     flops_bob = FLOPS_BOB * unit
     hbm, pk, pk_sus, pk_kind = peaks()
-    value = ws * flops_step / (step_ms * 1e-3) / 1e12
+    value = job_tflops(ws, flops_step, step_ms)
     bob_tf = flops_bob / (bob_ms * 1e-3) / 1e12
-    launches_per_step = 5
+    launches_per_step = 1 + 2 + (3 if w.d == 128 else 2)  # fwd, bwd (2), BoB (2 or 3)
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws,
@@ -227,7 +223,7 @@ def run_ours(args, w):
             "bob": {"ms_per_call": round(bob_ms, 4), "tflops": round(bob_tf, 3),
                     "frac_of_peak": round(bob_tf / pk, 4), "peak_tflops": pk, "peak_kind": pk_kind,
                     "counted_flops": flops_bob},
-            "e2e": {"value": round(ws * flops_step / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "e2e": {"value": round(job_tflops(ws, flops_step, e2e_ms), 3), "unit": "TFLOP/s",
                     "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
@@ -237,6 +233,39 @@ def run_ours(args, w):
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+def run_once(args, w):
+    """Profiler target: the same step as the timed loop, run warmup + 1 times."""
+    import torch
+
+    import attn_inputs
+    import exact_second_order_attn_gb300 as fb
+    fb.load()
+    x = {k: v.cuda() for k, v in attn_inputs.make_inputs(w).items()}
+    for _ in range(args.warmup + 1):
+        O, L = fb.attn_fwd(x["Q"], x["K"], x["V"], w.tau)
+        dQ, dK, dV, D = fb.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], L, w.tau)
+        fb.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], L, D, x["UQ"], x["UK"], x["UV"], w.tau)
+    fb.device_status()
+    torch.cuda.synchronize()
+    print(f"once ok: {w.name}")
+
+
+def reduce_max(v, world_size, device):
+    """Max of a per-rank float over all ranks (the slowest replica sets the time)."""
+    if world_size == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world_size, flops_per_rank_step, step_ms):
+    """Whole-job throughput: every replica does the same work; time is the max."""
+    return world_size * flops_per_rank_step / (step_ms * 1e-3) / 1e12
 
 
 def roofline(w, bob_ms, pk, pk_kind):
@@ -317,12 +346,16 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(attn_inputs.WORKLOADS))
     ap.add_argument("--cpu-rows", type=int, default=256,
                     help="query rows of one head per CPU-oracle sample")
+    ap.add_argument("--once", action="store_true",
+                    help="run --warmup + 1 steps and exit without timing (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     w = attn_inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.once:
+        run_once(args, w)
     else:
         run_ours(args, w)
 

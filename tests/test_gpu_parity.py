@@ -9,7 +9,9 @@ Tolerances (per output tensor, max|gpu - ref| / max|ref|):
   the closed-form reduction (evolve.pub review, Strengths: paper Lemma E.2).
 """
 
+import json
 import math
+import os
 
 import numpy as np
 import pytest
@@ -27,6 +29,20 @@ BF16_TOL = 1e-2
 FP32_TOL = 2e-5
 CLOSED_FORM_TOL = 1e-5
 KEYS = ("O", "L", "dQ", "dK", "dV", "D", "gQ", "gK", "gV", "gdO", "alpha", "E")
+# Identity residuals at any size: <gdO, dO> - f and <gV, V> - (<UQ,dQ> + <UK,dK>)
+# are random-sign sums of per-element errors, and so are the reference sums,
+# so their ratio is of the order of the per-element relative error: bf16
+# operand rounding (unit roundoff 2^-9) on the tensor-core path.  They are held
+# to the bf16 parity bar.
+IDENTITY_TOL = BF16_TOL
+
+
+def log_errors(case, errs):
+    """Append measured errors to $FBOB_PARITY_LOG (one JSON line per case)."""
+    path = os.environ.get("FBOB_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": case, **{k: float(v) for k, v in errs.items()}}) + "\n")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -36,8 +52,9 @@ def _lib():
     torch.cuda.init()
 
 
-def compare_all(gpu, ref, tol, keys=KEYS):
+def compare_all(gpu, ref, tol, keys=KEYS, case=None):
     errs = {k: rel_err(gpu[k], ref[k]) for k in keys}
+    log_errors(case or os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], errs)
     bad = {k: e for k, e in errs.items() if not (e <= tol)}
     assert not bad, f"over tolerance {tol}: {bad} (all: {errs})"
     return errs
@@ -120,8 +137,11 @@ def sampled_row_checks(w, gpu, inp, rows, head=(0, 0)):
     fk = (x["UK"] * g["dK"]).sum()
     fv = (x["UV"] * g["dV"]).sum()
     mag = abs(fq) + abs(fk) + abs(fv)
-    assert abs((g["gdO"] * x["dO"]).sum() - (fq + fk + fv)) <= 1e-3 * mag
-    assert abs((g["gV"] * x["V"]).sum() - (fq + fk)) <= 1e-3 * (abs(fq) + abs(fk))
+    r1 = abs((g["gdO"] * x["dO"]).sum() - (fq + fk + fv)) / mag
+    r2 = abs((g["gV"] * x["V"]).sum() - (fq + fk)) / (abs(fq) + abs(fk))
+    log_errors(os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0] + ":identities",
+               {**errs, "euler_gdO": r1, "euler_gV": r2})
+    assert r1 <= IDENTITY_TOL and r2 <= IDENTITY_TOL, (r1, r2)
     return errs
 
 
@@ -155,7 +175,9 @@ def test_closed_form_fp32():
     gpu, inp = run_chain(w)
     x = oracle_inputs(inp)
     expect, _ = orc.attn_fwd(x["Q"], x["K"], x["UV"], w.tau)
-    assert rel_err(gpu["gdO"], expect) <= CLOSED_FORM_TOL
+    err = rel_err(gpu["gdO"], expect)
+    log_errors("closed_form_fp32", {"gdO": err})
+    assert err <= CLOSED_FORM_TOL
     for k in ("gQ", "gK", "gV"):
         assert not np.any(gpu[k]), k
     rows = [0, 4097, w.N - 1]
