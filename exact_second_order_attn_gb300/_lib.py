@@ -23,7 +23,7 @@ BF16, FP32 = 0, 1
 FUNCTIONS = (
     "fbob_attn_fwd", "fbob_attn_bwd", "fbob_bob_workspace_bytes", "fbob_attn_bob",
     "fbob_device_status", "fbob_set_wait_limit_ns", "fbob_status_string", "fbob_last_error",
-    "fbob_abi_version",
+    "fbob_abi_version", "fbob_attn_bob_noalloc",
 )
 
 
@@ -59,6 +59,8 @@ def load():
     lib.fbob_bob_workspace_bytes.restype = ctypes.c_size_t
     lib.fbob_attn_bob.argtypes = [cp] + [vp] * 15 + [ctypes.c_size_t, vp]
     lib.fbob_attn_bob.restype = st
+    lib.fbob_attn_bob_noalloc.argtypes = [cp] + [vp] * 15
+    lib.fbob_attn_bob_noalloc.restype = st
     lib.fbob_device_status.argtypes = [vp]
     lib.fbob_device_status.restype = st
     lib.fbob_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
@@ -180,6 +182,23 @@ def fbob_attn_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ=None, gK=None, gV=No
                                 _ptr(UQ), _ptr(UK), _ptr(UV), _ptr(gQ), _ptr(gK), _ptr(gV), _ptr(gdO),
                                 _ptr(workspace), ctypes.c_size_t(nbytes), _stream(stream)))
     return gQ, gK, gV, gdO, workspace
+
+
+def fbob_attn_bob_noalloc(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ=None, gK=None, gV=None, gdO=None,
+                          stream=None):
+    """(gQ, gK, gV, gdO) = BoB with the library's fixed workspace (no workspace argument)."""
+    p = problem_for(Q, tau)
+    gQ = _empty(Q) if gQ is None else gQ
+    gK = _empty(Q) if gK is None else gK
+    gV = _empty(Q) if gV is None else gV
+    gdO = _empty(Q) if gdO is None else gdO
+    _same(Q, K, V, dO, UQ, UK, UV, dtype=Q.dtype, shape=Q.shape)
+    _same(Q, O, gQ, gK, gV, gdO, dtype=torch.float32, shape=Q.shape)
+    _same(Q, L, D, dtype=torch.float32, shape=Q.shape[:3])
+    _check(load().fbob_attn_bob_noalloc(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L),
+                                        _ptr(D), _ptr(UQ), _ptr(UK), _ptr(UV), _ptr(gQ), _ptr(gK), _ptr(gV),
+                                        _ptr(gdO), _stream(stream)))
+    return gQ, gK, gV, gdO
 
 
 def fbob_device_status(stream=None):

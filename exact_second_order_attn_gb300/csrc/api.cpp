@@ -162,6 +162,34 @@ fbob_status fbob_attn_bob(const fbob_problem* p, const void* Q, const void* K, c
   return FBOB_OK;
 }
 
+fbob_status fbob_attn_bob_noalloc(const fbob_problem* p, const void* Q, const void* K, const void* V,
+                                  const float* O, const void* dO, const float* L, const float* D, const void* UQ,
+                                  const void* UK, const void* UV, float* gQ, float* gK, float* gV, float* gdO,
+                                  cudaStream_t stream) {
+  bool empty = false;
+  fbob_status st = check_problem(p, &empty);
+  if (st != FBOB_OK) return st;
+  if (empty) return FBOB_OK;
+  const Ptr ps[] = {{Q, "Q"},   {K, "K"},   {V, "V"},   {O, "O"},   {dO, "dO"}, {L, "L"},    {D, "D"},
+                    {UQ, "UQ"}, {UK, "UK"}, {UV, "UV"}, {gQ, "gQ"}, {gK, "gK"}, {gV, "gV"}, {gdO, "gdO"}};
+  if ((st = check_ptrs(ps, 14)) != FBOB_OK) return st;
+  const size_t rows = (size_t)p->B * (size_t)p->H * (size_t)p->N;
+  if (rows > fbob::static_workspace_rows())
+    return fail(FBOB_ERR_UNSUPPORTED,
+                "fbob_attn_bob_noalloc: B*H*N = %zu exceeds the fixed workspace of %zu rows; "
+                "use fbob_attn_bob with a caller workspace",
+                rows, fbob::static_workspace_rows());
+  float* ws = nullptr;
+  cudaError_t e = fbob::static_workspace(&ws);
+  if (e != cudaSuccess) return cuda_fail(e, "fixed workspace address");
+  fbob::DevCtx c;
+  if ((st = make_ctx(&c)) != FBOB_OK) return st;
+  fbob::BobArgs a{Q, K, V, dO, UQ, UK, UV, O, L, D, gQ, gK, gV, gdO, ws, p->B * p->H, p->N, p->d, p->tau};
+  e = p->dtype == FBOB_BF16 ? fbob::tc_bob(a, c, stream) : fbob::simt_bob(a, c, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bob_noalloc launch");
+  return FBOB_OK;
+}
+
 fbob_status fbob_device_status(cudaStream_t stream) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");

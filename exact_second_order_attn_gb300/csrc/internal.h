@@ -55,4 +55,8 @@ cudaError_t tc_fwd(const FwdArgs& a, const DevCtx& c, cudaStream_t s);
 cudaError_t tc_bwd(const BwdArgs& a, const DevCtx& c, cudaStream_t s);
 cudaError_t tc_bob(const BobArgs& a, const DevCtx& c, cudaStream_t s);
 
+// bob_static.cu: the fixed (alpha, E) workspace of fbob_attn_bob_noalloc.
+size_t static_workspace_rows();           // capacity in query rows (B*H*N)
+cudaError_t static_workspace(float** ptr);  // device address on the current device
+
 }  // namespace fbob

@@ -133,6 +133,33 @@ fbob_status fbob_attn_bob(const fbob_problem* p,
                           cudaStream_t stream);
 
 /*
+ * BoB without a caller workspace (the paper has no counterpart; this is a
+ * convenience of this library).  Same inputs, outputs, passes and errors as
+ * fbob_attn_bob, but the (alpha, E) workspace is a fixed device array inside
+ * the library, so the caller passes only inputs and outputs and nothing is
+ * allocated.  It serves callers that cannot obtain an extra device buffer:
+ * hosts that hand over only their own tensors, or loops that must not call
+ * cudaMalloc/cudaFree (they can synchronise the device).
+ *   - Capacity: B*H*N <= 2097152 (2^21) query rows; larger problems return
+ *     FBOB_ERR_UNSUPPORTED before any launch.  Every GPU that loads the
+ *     library holds the array (16 MiB) until the process exits.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture on the device.
+ *   - All calls on a device share the array: calls whose kernels overlap on
+ *     the GPU (e.g. on two unordered streams) race and give wrong results.
+ *     Calls ordered on one stream are safe; no clearing is needed between
+ *     them (pass 1 rewrites every element pass 2 reads).
+ */
+fbob_status fbob_attn_bob_noalloc(const fbob_problem* p,
+                                  const void* Q, const void* K, const void* V,
+                                  const float* O, const void* dO,
+                                  const float* L, const float* D,
+                                  const void* UQ, const void* UK, const void* UV,
+                                  float* gQ, float* gK, float* gV, float* gdO,
+                                  cudaStream_t stream);
+
+/*
  * Device status: waits for `stream` to finish (this call DOES synchronise),
  * then returns FBOB_ERR_TIMEOUT if any kernel of this library on the current
  * device gave up on a bounded wait since the last call, else FBOB_OK (or
