@@ -38,6 +38,14 @@ sys.path.insert(0, ROOT)
 METRIC = "attn BoB ms/call and TFLOP/s vs N (bf16, d=64/128); % of BF16 tensor peak"
 FLOPS_FWD, FLOPS_BWD, FLOPS_BOB = 4, 10, 38   # x N^2 d per head
 DEFAULT_WORKLOAD = "wide_head_b2h16_n16384_d128"
+# Counted GEMMs (2 N^2 d FLOPs each, per head) attributed to each kernel: the
+# 38 N^2 d of BoB = pass 1 (11: S, dP, C, B x2, U1 x2, U2, W, Y x2) + pass 2
+# (8); at d=128 pass 1 runs as a Q-side kernel (9) and a dO-side kernel (Y: 2;
+# its recomputed S and B are not counted).  Forward 2 (S, PV); first backward
+# 5 (S, dP, dQ in the row kernel, dV, dK in the column kernel; the column
+# kernel's recomputed S and dP are not counted).
+COUNTED_GEMMS = {"bob_pass1": 11, "bob_pass1_qside": 9, "bob_pass1_doside": 2, "bob_pass2": 8,
+                 "attn_fwd": 2, "attn_bwd_dq": 3, "attn_bwd_dkdv": 2}
 
 
 def peaks():
@@ -154,6 +162,8 @@ def run_ours(args, w):
 
     clocks = Clocks(local)
     clocks.start()
+    fb.fbob_profile_report()          # drop anything recorded so far
+    fb.fbob_profile_enable(True)      # per-kernel CUDA events on the launching stream
     barrier()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -162,6 +172,8 @@ def run_ours(args, w):
     t1.record(stream)
     barrier()
     clk = clocks.stop()
+    fb.fbob_profile_enable(False)
+    kernels = fb.fbob_profile_report()
     step_ms = max_over_ranks(t0.elapsed_time(t1) / args.steps)
     fb.device_status()
 
@@ -228,7 +240,8 @@ def run_ours(args, w):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
-        line["roofline"] = roofline(w, bob_ms, pk, pk_kind)
+        line["kernels"] = {k: {"launches": v[0], "avg_ms": round(v[1] / v[0], 4)} for k, v in kernels.items()}
+        line["roofline"] = roofline(w, kernels, pk_sus)
         line["cpu_baseline"] = cpu_baseline(w, args, head0(host))
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -268,12 +281,44 @@ def job_tflops(world_size, flops_per_rank_step, step_ms):
     return world_size * flops_per_rank_step / (step_ms * 1e-3) / 1e12
 
 
-def roofline(w, bob_ms, pk, pk_kind):
-    unit = w.N * w.N * w.d * w.B * w.H
-    achieved = FLOPS_BOB * unit / (bob_ms * 1e-3) / 1e12
-    return {"kernel": "attn_bob (pass 1 + pass 2)", "bound": "tensor", "achieved": round(achieved, 3),
-            "peak": pk, "unit": "TFLOP/s", "frac": round(achieved / pk, 4), "traffic": None,
-            "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({pk_kind})"}
+def kernel_source_hash():
+    """Hash of the tensor-core kernel sources; DRAM counters taken with other
+    sources are stale."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_second_order_attn_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.startswith("tc_") or f == "tmap.cu":
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def roofline(w, kernels, peak):
+    """Roofline of the dominant kernel (largest share of the timed region):
+    counted FLOPs per launch / its average launch time (CUDA events recorded by
+    the library on the launching stream during the timed loop), against the
+    sustained bf16 peak (the kernel runs inside a long step).  traffic = DRAM
+    bytes per launch from the committed ncu summary, scaled from its profiling
+    workload by the number of heads, or null if the kernels changed since."""
+    if not kernels:
+        return None
+    name, (n, total, _, _) = max(kernels.items(), key=lambda kv: kv[1][1])
+    avg_ms = total / n
+    flops = COUNTED_GEMMS.get(name, 0) * 2 * w.N * w.N * w.d * w.B * w.H
+    achieved = flops / (avg_ms * 1e-3) / 1e12
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            rec = json.load(f)
+        k = rec["kernels"].get(name)
+        if k and rec.get("source_hash") == kernel_source_hash() and k["d"] == w.d and k["N"] == w.N:
+            traffic = k["bytes_per_launch"] * (w.B * w.H) / k["heads"]
+    except (OSError, KeyError, ValueError):
+        traffic = None
+    return {"kernel": name, "bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+            "avg_launch_ms": round(avg_ms, 4), "counted_flops_per_launch": flops,
+            "peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained (kernel timed inside the step)"}
 
 
 def head0(inp):
@@ -302,7 +347,7 @@ def blas_threads():
 
 
 def cpu_baseline(w, args, x):
-    rows = args.cpu_rows
+    rows = args.baseline_rows
     secs = oracle_sample(w, x, rows)
     flops = (FLOPS_FWD + FLOPS_BWD + FLOPS_BOB) * rows * w.N * w.d
     return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(),
@@ -340,12 +385,14 @@ def main():
     import attn_inputs
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(attn_inputs.WORKLOADS))
-    ap.add_argument("--cpu-rows", type=int, default=256,
-                    help="query rows of one head per CPU-oracle sample")
+    ap.add_argument("--cpu-rows", type=int, default=2048,
+                    help="query rows of one head per reference-arm step (CPU oracle)")
+    ap.add_argument("--baseline-rows", type=int, default=8192,
+                    help="query rows of one head in the cpu_baseline sample")
     ap.add_argument("--once", action="store_true",
                     help="run --warmup + 1 steps and exit without timing (for profiler captures)")
     args = ap.parse_args()

@@ -23,7 +23,8 @@ BF16, FP32 = 0, 1
 FUNCTIONS = (
     "fbob_attn_fwd", "fbob_attn_bwd", "fbob_bob_workspace_bytes", "fbob_attn_bob",
     "fbob_device_status", "fbob_set_wait_limit_ns", "fbob_status_string", "fbob_last_error",
-    "fbob_abi_version", "fbob_attn_bob_noalloc",
+    "fbob_abi_version", "fbob_attn_bob_noalloc", "fbob_profile_enable", "fbob_profile_report",
+    "fbob_debug_stall_producer",
 )
 
 
@@ -69,6 +70,12 @@ def load():
     lib.fbob_status_string.restype = ctypes.c_char_p
     lib.fbob_last_error.argtypes = []
     lib.fbob_last_error.restype = ctypes.c_char_p
+    lib.fbob_profile_enable.argtypes = [ctypes.c_int]
+    lib.fbob_profile_enable.restype = ctypes.c_int
+    lib.fbob_profile_report.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
+    lib.fbob_profile_report.restype = ctypes.c_int
+    lib.fbob_debug_stall_producer.argtypes = [ctypes.c_int]
+    lib.fbob_debug_stall_producer.restype = ctypes.c_int
     lib.fbob_abi_version.argtypes = []
     lib.fbob_abi_version.restype = ctypes.c_int
     _lib = lib
@@ -208,6 +215,23 @@ def fbob_device_status(stream=None):
 
 def fbob_set_wait_limit_ns(ns: int) -> int:
     return int(load().fbob_set_wait_limit_ns(ctypes.c_ulonglong(ns)))
+
+
+def fbob_profile_enable(on: bool) -> bool:
+    return bool(load().fbob_profile_enable(int(bool(on))))
+
+
+def fbob_profile_report() -> dict:
+    """Per-kernel {name: (launches, total_ms, min_ms, max_ms)} since the last report."""
+    import json
+    n = load().fbob_profile_report(None, 0)
+    buf = ctypes.create_string_buffer(n + 1)
+    load().fbob_profile_report(buf, n + 1)
+    return {k: tuple(v) for k, v in json.loads(buf.value.decode()).items()}
+
+
+def fbob_debug_stall_producer(stall: bool) -> bool:
+    return bool(load().fbob_debug_stall_producer(int(bool(stall))))
 
 
 def fbob_abi_version() -> int:

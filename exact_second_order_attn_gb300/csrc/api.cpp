@@ -16,6 +16,7 @@ namespace {
 
 thread_local char g_last_error[512] = "";
 std::atomic<unsigned long long> g_wait_ns{2000000000ull};
+std::atomic<int> g_stall{0};
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 
 fbob_status fail(fbob_status s, const char* fmt, ...) {
@@ -72,6 +73,7 @@ fbob_status make_ctx(fbob::DevCtx* c) {
   cudaError_t e = fbob::dev_status_word(&c->err);
   if (e != cudaSuccess) return cuda_fail(e, "device status word");
   c->wait_ns = g_wait_ns.load();
+  c->stall = g_stall.load();
   return FBOB_OK;
 }
 
@@ -98,6 +100,8 @@ const char* fbob_last_error(void) { return g_last_error; }
 unsigned long long fbob_set_wait_limit_ns(unsigned long long ns) {
   return g_wait_ns.exchange(ns == 0 ? kDefaultWaitNs : ns);
 }
+
+int fbob_debug_stall_producer(int stall) { return g_stall.exchange(stall ? 1 : 0); }
 
 size_t fbob_bob_workspace_bytes(const fbob_problem* p) {
   if (!p || p->B < 0 || p->H < 0 || p->N < 0) return 0;

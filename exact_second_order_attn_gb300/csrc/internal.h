@@ -13,6 +13,7 @@ namespace fbob {
 struct DevCtx {
   unsigned int* err;           // device address of the status word
   unsigned long long wait_ns;  // per-wait time limit
+  int stall;                   // test hook: producer withholds its first tile
 };
 
 struct FwdArgs {
@@ -50,7 +51,7 @@ cudaError_t simt_fwd(const FwdArgs& a, const DevCtx& c, cudaStream_t s);
 cudaError_t simt_bwd(const BwdArgs& a, const DevCtx& c, cudaStream_t s);
 cudaError_t simt_bob(const BobArgs& a, const DevCtx& c, cudaStream_t s);
 
-// tc_attn.cu / tc_bob.cu: tcgen05 kernels for bf16 inputs (N % 128 == 0).
+// tc_fwd.cu / tc_bwd.cu / tc_bob.cu: tcgen05 kernels for bf16 inputs (N % 128 == 0).
 cudaError_t tc_fwd(const FwdArgs& a, const DevCtx& c, cudaStream_t s);
 cudaError_t tc_bwd(const BwdArgs& a, const DevCtx& c, cudaStream_t s);
 cudaError_t tc_bob(const BobArgs& a, const DevCtx& c, cudaStream_t s);

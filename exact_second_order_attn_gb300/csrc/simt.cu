@@ -19,6 +19,7 @@
 #include <math.h>
 
 #include "internal.h"
+#include "prof.h"
 
 namespace fbob {
 namespace {
@@ -490,29 +491,31 @@ template <int D> constexpr size_t p2_smem() {
 }
 
 template <typename Args, typename Kern>
-cudaError_t go(Kern kernel, size_t smem, int N, int BH, const Args& args, cudaStream_t s) {
+cudaError_t go(const char* name, Kern kernel, size_t smem, int N, int BH, const Args& args, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((N + BR - 1) / BR, BH);
+  prof_begin(s, name);
   kernel<<<grid, NT, smem, s>>>(args);
+  prof_end(s);
   return cudaGetLastError();
 }
 
 template <typename T, int D>
 cudaError_t fwd_t(const FwdArgs& a, cudaStream_t s) {
-  return go(simt_fwd_kernel<T, D>, fwd_smem<D>(), a.N, a.BH, a, s);
+  return go("simt_fwd", simt_fwd_kernel<T, D>, fwd_smem<D>(), a.N, a.BH, a, s);
 }
 template <typename T, int D>
 cudaError_t bwd_t(const BwdArgs& a, cudaStream_t s) {
-  cudaError_t e = go(simt_bwd_dq_kernel<T, D>, dq_smem<D>(), a.N, a.BH, a, s);
+  cudaError_t e = go("simt_bwd_dq", simt_bwd_dq_kernel<T, D>, dq_smem<D>(), a.N, a.BH, a, s);
   if (e != cudaSuccess) return e;
-  return go(simt_bwd_dkdv_kernel<T, D>, dkdv_smem<D>(), a.N, a.BH, a, s);
+  return go("simt_bwd_dkdv", simt_bwd_dkdv_kernel<T, D>, dkdv_smem<D>(), a.N, a.BH, a, s);
 }
 template <typename T, int D>
 cudaError_t bob_t(const BobArgs& a, cudaStream_t s) {
-  cudaError_t e = go(simt_bob_pass1_kernel<T, D>, p1_smem<D>(), a.N, a.BH, a, s);
+  cudaError_t e = go("simt_bob_pass1", simt_bob_pass1_kernel<T, D>, p1_smem<D>(), a.N, a.BH, a, s);
   if (e != cudaSuccess) return e;
-  return go(simt_bob_pass2_kernel<T, D>, p2_smem<D>(), a.N, a.BH, a, s);
+  return go("simt_bob_pass2", simt_bob_pass2_kernel<T, D>, p2_smem<D>(), a.N, a.BH, a, s);
 }
 
 }  // namespace

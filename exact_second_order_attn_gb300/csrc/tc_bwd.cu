@@ -1,0 +1,313 @@
+// Tensor-core (tcgen05 + TMEM + TMA) first backward for bf16 inputs, d in
+// {64, 128}, N a multiple of 128, on the tile skeleton of tc_tile.cuh.  It
+// produces dQ, dK, dV and D = rowsum(dO o O), the row term BoB reads.
+//
+// Source: "FlashBoB: I/O-Efficient Exact Backward-over-Backward for Softmax
+// Attention" - the abstract (the FlashAttention-style first backward that BoB
+// differentiates through) and the evolve.pub review FAQ "What is
+// backward-over-backward (BoB)" (BoB is the vector-Jacobian product of this map).
+//
+//   row kernel (128 query rows): D = rowsum(dO o O); S = Q K^T, dP = dO V^T;
+//     dS = P (dP - D); dQ += dS K; dQ *= tau.
+//   column kernel (128 keys): S^T = K Q^T, dP^T = V dO^T; dV += P^T dO;
+//     dK += dS^T Q; dK *= tau.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "prof.h"
+#include "tc_tile.cuh"
+
+namespace fbob {
+namespace {
+
+using namespace tc;
+using tile::kM;
+using tile::kT;
+
+// ===========================================================================
+// first backward on the tile skeleton
+// ===========================================================================
+struct DqParams {
+  CUtensorMap mQ, mdO;     // resident
+  CUtensorMap mK, mV;      // streamed
+  const float *O, *L;
+  const __nv_bfloat16* dO;
+  float *dQ, *D;
+  int N;
+  float tau;
+  unsigned int* err;
+  unsigned long long wait_ns;
+  int stall;
+};
+
+// Row kernel: resident Q, dO; ring A = K (read by dQ += dS K), ring B = V
+// (read only by dP = dO V^T).  dS goes to TMEM (TS MMA).
+template <int D_>
+struct DqOp {
+  using Params = DqParams;
+  static constexpr int D = D_, DC = D / 64;
+  static constexpr int RES = 2 * DC * tile::kChunk;
+  static constexpr int ACH = tile::kBlk, BCH = tile::kBlk;
+  static constexpr int SA = DC * ACH, SB = DC * BCH, SA_TX = SA, SB_TX = SB;
+  static constexpr int NSA = 4, NSB = 4;
+  static constexpr bool VEC = false, ROW_SUMS = false, TS = true;
+  static constexpr int VEC_OFF = 0, OPS = 0;
+  static constexpr int ACC = D, SCOLS = 64, NBUF = 2;   // [S | dP]
+  static constexpr int OP_HALF = 16, OP_COL = ACC + NBUF * SCOLS;
+  static constexpr int SMEM = RES + NSA * SA + NSB * SB;
+  static_assert(OP_COL + 2 * OP_HALF <= 512, "TMEM budget");
+  static_assert(SMEM + 1024 <= 232448, "shared memory budget");
+
+  __device__ static void load_res(const Params& p, uint8_t* res, uint64_t* bar, int row0, int head) {
+    for (int kc = 0; kc < DC; ++kc) {
+      tma_load_3d(res + kc * tile::kChunk, &p.mQ, bar, kc * 64, row0, head);
+      tma_load_3d(res + (DC + kc) * tile::kChunk, &p.mdO, bar, kc * 64, row0, head);
+    }
+  }
+  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
+    for (int kc = 0; kc < DC; ++kc) tma_load_3d(st + kc * ACH, &p.mK, bar, kc * 64, t * tile::kT, head);
+  }
+  __device__ static void load_b(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
+    for (int kc = 0; kc < DC; ++kc) tma_load_3d(st + kc * BCH, &p.mV, bar, kc * 64, t * tile::kT, head);
+  }
+  __device__ static void score_mmas(uint32_t sc, uint32_t res, uint32_t sa, uint32_t sb) {
+    const uint32_t i32 = idesc_bf16(tile::kM, 32, false, false);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      mma_ss(sc, tile::res_desc(res, 0, DC, k), tile::stage_kdesc(sa, ACH, 0, k), i32, k > 0);       // S
+      mma_ss(sc + 32, tile::res_desc(res, 1, DC, k), tile::stage_kdesc(sb, BCH, 0, k), i32, k > 0);  // dP
+    }
+  }
+  __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
+    const uint32_t id = idesc_bf16(tile::kM, D, false, true);
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk)
+      mma_ts(tb, ops + h * OP_HALF + kk * 8, tile::stage_mndesc(sa, ACH, 0, kk), id,
+             (first && kk == 0) ? 0u : 1u);  // dQ += dS K
+  }
+  struct Row {
+    float nL, Di;
+  };
+  __device__ static void ew_init(Row& w, const Params& p, int blk0, int r, int head) {
+    const size_t vo = (size_t)head * p.N + blk0 + r;
+    const size_t ro = vo * D;
+    // D_i = rowsum(dO o O) of this thread's row
+    float Di = 0.f;
+    const uint4* g = reinterpret_cast<const uint4*>(p.dO + ro);
+    const float4* o = reinterpret_cast<const float4*>(p.O + ro);
+#pragma unroll 4
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 u = g[c];
+      const float4 o0 = o[2 * c], o1 = o[2 * c + 1];
+      const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&u);
+      const float2 a0 = __bfloat1622float2(hb[0]), a1 = __bfloat1622float2(hb[1]);
+      const float2 a2 = __bfloat1622float2(hb[2]), a3 = __bfloat1622float2(hb[3]);
+      Di = fmaf(a0.x, o0.x, Di);
+      Di = fmaf(a0.y, o0.y, Di);
+      Di = fmaf(a1.x, o0.z, Di);
+      Di = fmaf(a1.y, o0.w, Di);
+      Di = fmaf(a2.x, o1.x, Di);
+      Di = fmaf(a2.y, o1.y, Di);
+      Di = fmaf(a3.x, o1.z, Di);
+      Di = fmaf(a3.y, o1.w, Di);
+    }
+    if (threadIdx.x < 128) p.D[vo] = Di;  // one of the two warpgroups writes it
+    w.Di = Di;
+    w.nL = -p.L[vo] * tile::kLog2e;
+  }
+  __device__ static bool ew_tile(Row& w, const Params& p, const tile::TileArgs& a, const tile::TileSync& s, int) {
+    const float sc = p.tau * tile::kLog2e;
+    uint32_t wd[16];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      float S[16], dP[16];
+      tmem_ld16x2(a.sc + q * 16, a.sc + 32 + q * 16, S, dP);
+      if (q == 1) s.release_scores();
+#pragma unroll
+      for (int j = 0; j < 16; j += 2) {
+        const float p0 = tile::ex2(fmaf(S[j], sc, w.nL)), p1 = tile::ex2(fmaf(S[j + 1], sc, w.nL));
+        wd[q * 8 + j / 2] = pack_bf16x2(p0 * (dP[j] - w.Di), p1 * (dP[j + 1] - w.Di));
+      }
+    }
+    if (!s.acquire_ops()) return false;
+    tmem_st16_nowait(a.ops, wd);
+    s.publish_ops();
+    return true;
+  }
+  __device__ static void epilogue(Row&, const Params& p, const tile::EpiArgs& e) {
+    const size_t ro = ((size_t)e.head * p.N + e.blk0 + e.r) * D;
+    const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
+#pragma unroll 1
+    for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+      float v[16];
+      tmem_ld16(e.tm + c0, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] *= p.tau;
+      tile::store16(p.dQ + ro + c0, v);
+    }
+  }
+};
+
+struct DkvParams {
+  CUtensorMap mK, mV;      // resident
+  CUtensorMap mQ, mdO;     // streamed
+  const float *L, *D;
+  float *dK, *dV;
+  int N;
+  float tau;
+  unsigned int* err;
+  unsigned long long wait_ns;
+  int stall;
+};
+
+// Column kernel: resident K, V; ring A = [Q | dO] + (L, D) of the tile.
+// P and dS go to TMEM (TS MMAs).
+template <int D_>
+struct DkvOp {
+  using Params = DkvParams;
+  static constexpr int D = D_, DC = D / 64;
+  static constexpr int RES = 2 * DC * tile::kChunk;
+  static constexpr int ACH = 2 * tile::kBlk, VEC_OFF = DC * ACH;
+  static constexpr int SA = DC * ACH + 1024, SA_TX = DC * ACH + 256, SB = 0, SB_TX = 0;
+  static constexpr int NSA = 4, NSB = 0;
+  static constexpr bool VEC = true, ROW_SUMS = false, TS = true;
+  static constexpr int OPS = 0;
+  static constexpr int ACC = 2 * D, SCOLS = 64, NBUF = 2;   // dK, dV; [S^T | dP^T]
+  static constexpr int OP_HALF = 32, OP_COL = ACC + NBUF * SCOLS;
+  static constexpr int SMEM = RES + NSA * SA;
+  static_assert(OP_COL + 2 * OP_HALF <= 512, "TMEM budget");
+  static_assert(SMEM + 1024 <= 232448, "shared memory budget");
+
+  __device__ static void load_res(const Params& p, uint8_t* res, uint64_t* bar, int col0, int head) {
+    for (int kc = 0; kc < DC; ++kc) {
+      tma_load_3d(res + kc * tile::kChunk, &p.mK, bar, kc * 64, col0, head);
+      tma_load_3d(res + (DC + kc) * tile::kChunk, &p.mV, bar, kc * 64, col0, head);
+    }
+  }
+  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
+    for (int kc = 0; kc < DC; ++kc) {
+      tma_load_3d(st + kc * ACH, &p.mQ, bar, kc * 64, t * tile::kT, head);
+      tma_load_3d(st + kc * ACH + tile::kBlk, &p.mdO, bar, kc * 64, t * tile::kT, head);
+    }
+    const size_t v = (size_t)head * p.N + (size_t)t * tile::kT;
+    tile::bulk_load(st + VEC_OFF, p.L + v, 128, bar);
+    tile::bulk_load(st + VEC_OFF + 128, p.D + v, 128, bar);
+  }
+  __device__ static void load_b(const Params&, uint8_t*, uint64_t*, int, int) {}
+  __device__ static void score_mmas(uint32_t sc, uint32_t res, uint32_t sa, uint32_t) {
+    const uint32_t i32 = idesc_bf16(tile::kM, 32, false, false);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      mma_ss(sc, tile::res_desc(res, 0, DC, k), tile::stage_kdesc(sa, ACH, 0, k), i32, k > 0);       // S^T
+      mma_ss(sc + 32, tile::res_desc(res, 1, DC, k), tile::stage_kdesc(sa, ACH, 1, k), i32, k > 0);  // dP^T
+    }
+  }
+  __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
+    const uint32_t id = idesc_bf16(tile::kM, D, false, true);
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
+      const uint32_t a = ops + h * OP_HALF + kk * 8;
+      mma_ts(tb + D, a, tile::stage_mndesc(sa, ACH, 1, kk), id, acc0);   // dV += P^T dO
+      mma_ts(tb, a + 16, tile::stage_mndesc(sa, ACH, 0, kk), id, acc0);  // dK += dS^T Q
+    }
+  }
+  struct Row {};
+  __device__ static void ew_init(Row&, const Params&, int, int, int) {}
+  __device__ static bool ew_tile(Row&, const Params& p, const tile::TileArgs& a, const tile::TileSync& s, int) {
+    const float sc = p.tau * tile::kLog2e;
+    const float* vL = a.vec;
+    const float* vD = a.vec + 32;
+    uint32_t wP[16], wd[16];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      float S[16], dP[16];
+      tmem_ld16x2(a.sc + q * 16, a.sc + 32 + q * 16, S, dP);
+      if (q == 1) s.release_scores();
+#pragma unroll
+      for (int c = 0; c < 16; c += 2) {
+        const int ii = q * 16 + c;
+        const float p0 = tile::ex2(fmaf(S[c], sc, -vL[ii] * tile::kLog2e));
+        const float p1 = tile::ex2(fmaf(S[c + 1], sc, -vL[ii + 1] * tile::kLog2e));
+        wP[q * 8 + c / 2] = pack_bf16x2(p0, p1);
+        wd[q * 8 + c / 2] = pack_bf16x2(p0 * (dP[c] - vD[ii]), p1 * (dP[c + 1] - vD[ii + 1]));
+      }
+    }
+    if (!s.acquire_ops()) return false;
+    tmem_st16_nowait(a.ops, wP);
+    tmem_st16_nowait(a.ops + 16, wd);
+    s.publish_ops();
+    return true;
+  }
+  __device__ static void epilogue(Row&, const Params& p, const tile::EpiArgs& e) {
+    const size_t ro = ((size_t)e.head * p.N + e.blk0 + e.r) * D;
+    const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
+#pragma unroll 1
+    for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+      float k_[16], v[16];
+      tmem_ld16x2(e.tm + c0, e.tm + D + c0, k_, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) k_[j] *= p.tau;
+      tile::store16(p.dK + ro + c0, k_);
+      tile::store16(p.dV + ro + c0, v);
+    }
+  }
+};
+
+// ===========================================================================
+// host side
+// ===========================================================================
+template <typename K, typename Params>
+cudaError_t launch(const char* name, K kernel, int smem, int threads, dim3 grid, const Params& prm, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  prof_begin(s, name);
+  kernel<<<grid, threads, smem, s>>>(prm);
+  prof_end(s);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
+  DqParams q;
+  if (!make_bf16_map(&q.mQ, a.Q, a.BH, a.N, D, kM) || !make_bf16_map(&q.mdO, a.dO, a.BH, a.N, D, kM) ||
+      !make_bf16_map(&q.mK, a.K, a.BH, a.N, D, kT) || !make_bf16_map(&q.mV, a.V, a.BH, a.N, D, kT))
+    return cudaErrorInvalidValue;
+  q.O = a.O;
+  q.L = a.L;
+  q.dO = static_cast<const __nv_bfloat16*>(a.dO);
+  q.dQ = a.dQ;
+  q.D = a.D;
+  q.N = a.N;
+  q.tau = a.tau;
+  q.err = c.err;
+  q.wait_ns = c.wait_ns;
+  q.stall = c.stall;
+  const dim3 grid(a.N / kM, a.BH);
+  cudaError_t e = launch("attn_bwd_dq", tile::tile_kernel<DqOp<D>>, DqOp<D>::SMEM, tile::kThreads, grid, q, s);
+  if (e != cudaSuccess) return e;
+  DkvParams k;
+  if (!make_bf16_map(&k.mK, a.K, a.BH, a.N, D, kM) || !make_bf16_map(&k.mV, a.V, a.BH, a.N, D, kM) ||
+      !make_bf16_map(&k.mQ, a.Q, a.BH, a.N, D, kT) || !make_bf16_map(&k.mdO, a.dO, a.BH, a.N, D, kT))
+    return cudaErrorInvalidValue;
+  k.L = a.L;
+  k.D = a.D;
+  k.dK = a.dK;
+  k.dV = a.dV;
+  k.N = a.N;
+  k.tau = a.tau;
+  k.err = c.err;
+  k.wait_ns = c.wait_ns;
+  k.stall = c.stall;
+  return launch("attn_bwd_dkdv", tile::tile_kernel<DkvOp<D>>, DkvOp<D>::SMEM, tile::kThreads, grid, k, s);
+}
+
+}  // namespace
+
+cudaError_t tc_bwd(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
+  return a.d == 64 ? bwd_d<64>(a, c, s) : bwd_d<128>(a, c, s);
+}
+
+}  // namespace fbob

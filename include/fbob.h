@@ -174,6 +174,28 @@ fbob_status fbob_device_status(cudaStream_t stream);
  */
 unsigned long long fbob_set_wait_limit_ns(unsigned long long ns);
 
+/*
+ * Per-kernel timing (measurement aid, off by default).  While enabled, every
+ * kernel launch of the library is bracketed by two CUDA events recorded on
+ * its stream.  fbob_profile_report waits for the recorded launches, adds
+ * them to per-kernel totals and returns the length of the text
+ * {"kernel": [launches, total_ms, min_ms, max_ms], ...}; if buf can hold the
+ * whole text (len > length) it writes it NUL-terminated and clears the
+ * totals, otherwise (e.g. buf == NULL) the totals are kept.
+ * fbob_profile_enable returns the previous setting.
+ */
+int fbob_profile_enable(int on);
+int fbob_profile_report(char* buf, size_t len);
+
+/*
+ * Test hook for the give-up path (off by default).  With stall = 1 the TMA
+ * producer of every tensor-core kernel launched afterwards withholds its
+ * first streamed tile, so the consumers' bounded waits run out: the kernels
+ * give up, free their resources and return, and fbob_device_status reports
+ * FBOB_ERR_TIMEOUT.  Returns the previous setting.
+ */
+int fbob_debug_stall_producer(int stall);
+
 /* Static text for a status code. */
 const char* fbob_status_string(fbob_status s);
 

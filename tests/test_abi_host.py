@@ -132,3 +132,18 @@ def test_binding_raises_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         _lib.load()
+
+
+def test_profile_report_empty_and_toggles(lib):
+    assert lib.fbob_profile_enable(0) in (0, 1)
+    n = lib.fbob_profile_report(None, 0)
+    buf = ctypes.create_string_buffer(n + 1)
+    assert lib.fbob_profile_report(buf, n + 1) == n
+    assert buf.value.decode() == "{}"
+    assert lib.fbob_profile_enable(1) == 0
+    assert lib.fbob_profile_enable(0) == 1
+
+
+def test_stall_hook_toggles_and_defaults_off(lib):
+    assert lib.fbob_debug_stall_producer(1) == 0
+    assert lib.fbob_debug_stall_producer(0) == 1

@@ -1,0 +1,77 @@
+"""The two-pass schedule the kernels run, restated tile by tile in fp64 NumPy
+and checked against the node-by-node reverse-mode oracle (CPU only).
+
+This pins the reformulation the CUDA kernels use (not the oracle): pass 1
+accumulates the alpha-free sums U1 = dS UK + X K, U2 = P K, W = dS K and
+Y = P UV + (P o B) V over key tiles together with alpha = sum P B and
+EX = sum X, and corrects them at the row end,
+    gQ = tau (U1 - EX U2 - alpha W),  gdO = Y - alpha O,  E = EX + D alpha;
+pass 2 recomputes each tile with the final alpha, E,
+    Gs = P (C + (B - alpha) (dP - D) + alpha D - E),  Gdp = P (B - alpha),
+    gK = tau (dS^T UQ + Gs^T Q),  gV = Gdp^T dO.
+(evolve.pub review, Summary and Key claims: two row scalars alpha, E, two
+passes; Strengths: alpha-free accumulators corrected after the reduction.)
+"""
+
+import numpy as np
+import pytest
+
+import oracle.attention as orc
+
+
+def two_pass(Q, K, V, dO, UQ, UK, UV, tau, L, O, D, br=16, bc=8):
+    N, d = Q.shape
+    gQ, gdO = np.zeros_like(Q), np.zeros_like(Q)
+    alpha, E = np.zeros(N), np.zeros(N)
+    for i0 in range(0, N, br):                      # pass 1: row blocks
+        r = slice(i0, min(N, i0 + br))
+        U1 = np.zeros((r.stop - r.start, d)); U2 = np.zeros_like(U1); W = np.zeros_like(U1); Y = np.zeros_like(U1)
+        a = np.zeros(r.stop - r.start); ex = np.zeros_like(a)
+        for j0 in range(0, N, bc):                  # loop over key tiles
+            c = slice(j0, min(N, j0 + bc))
+            P = np.exp(tau * Q[r] @ K[c].T - L[r, None])
+            B = tau * (UQ[r] @ K[c].T + Q[r] @ UK[c].T)
+            dP = dO[r] @ V[c].T
+            C = dO[r] @ UV[c].T
+            t = dP - D[r, None]
+            dS, X, PB = P * t, P * (C + B * t), P * B
+            a += PB.sum(1); ex += X.sum(1)
+            U1 += dS @ UK[c] + X @ K[c]; U2 += P @ K[c]; W += dS @ K[c]; Y += P @ UV[c] + PB @ V[c]
+        gQ[r] = tau * (U1 - ex[:, None] * U2 - a[:, None] * W)
+        gdO[r] = Y - a[:, None] * O[r]
+        alpha[r], E[r] = a, ex + D[r] * a
+    gK, gV = np.zeros_like(K), np.zeros_like(V)
+    for j0 in range(0, N, br):                      # pass 2: key blocks
+        c = slice(j0, min(N, j0 + br))
+        AK = np.zeros((c.stop - c.start, d)); AV = np.zeros_like(AK)
+        for i0 in range(0, N, bc):                  # loop over query tiles
+            r = slice(i0, min(N, i0 + bc))
+            Pt = np.exp(tau * K[c] @ Q[r].T - L[None, r])
+            Bt = tau * (UK[c] @ Q[r].T + K[c] @ UQ[r].T)
+            dPt = V[c] @ dO[r].T
+            Ct = UV[c] @ dO[r].T
+            t = dPt - D[None, r]
+            bp = Bt - alpha[None, r]
+            dSt = Pt * t
+            Gs = Pt * (Ct + bp * t + (alpha * D - E)[None, r])
+            Gd = Pt * bp
+            AK += dSt @ UQ[r] + Gs @ Q[r]; AV += Gd @ dO[r]
+        gK[c], gV[c] = tau * AK, AV
+    return gQ, gK, gV, gdO, alpha, E
+
+
+@pytest.mark.parametrize("N,d,sig", [(40, 8, (1,) * 7), (33, 5, (4, 4, 1, 1, 1, 1, 1)), (64, 16, (1, 1, 1, .1, .1, .1, .1))])
+def test_two_pass_schedule_matches_node_by_node_oracle(N, d, sig):
+    rng = np.random.default_rng(N * d)
+    X = [rng.standard_normal((N, d)) * s for s in sig]
+    Q, K, V, dO, UQ, UK, UV = X
+    tau = 1.0 / np.sqrt(d)
+    O, L = orc.attn_fwd_head(Q, K, V, tau)
+    _, _, _, D = orc.attn_bwd_rows(Q, K, V, dO, tau)
+    got = two_pass(Q, K, V, dO, UQ, UK, UV, tau, L, O, D)
+    ref = orc.bob_rows(Q, K, V, dO, UQ, UK, UV, tau)
+    for g, r in zip(got[:4], (ref[0], ref[1], ref[2], ref[3])):
+        np.testing.assert_allclose(g, r, rtol=1e-10, atol=1e-12)
+    alpha, E = orc.row_scalars(Q, K, V, dO, UQ, UK, UV, tau)
+    np.testing.assert_allclose(got[4], alpha, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(got[5], E, rtol=1e-10, atol=1e-12)
