@@ -142,37 +142,38 @@ struct Pass1 {
     const uint32_t i64 = idesc_bf16(kM, 64, false, false), i32 = idesc_bf16(kM, 32, false, false);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k)  // [S | Q UK^T] = Q [K; UK]^T
-      mma_ss(sc, res_desc(res, 0, DC, k), stage_kdesc(kst, kch, K_BLK, k), i64, k > 0);
+      mma_ss_w(sc, res_lo(res, 0, DC, k), kmaj_lo(kst, kch, K_BLK, k), i64, k > 0);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k)  // B += UQ K^T
-      mma_ss(sc + 32, res_desc(res, 1, DC, k), stage_kdesc(kst, kch, K_BLK, k), i32, 1);
+      mma_ss_w(sc + 32, res_lo(res, 1, DC, k), kmaj_lo(kst, kch, K_BLK, k), i32, 1);
     if (kQ) {
 #pragma unroll
       for (int k = 0; k < D / 16; ++k)  // [dP | C] = dO [V; UV]^T
-        mma_ss(sc + 64, res_desc(res, 2, DC, k), stage_kdesc(vst, vch, V_BLK, k), i64, k > 0);
+        mma_ss_w(sc + 64, res_lo(res, 2, DC, k), kmaj_lo(vst, vch, V_BLK, k), i64, k > 0);
     }
   }
 
   __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
+    const uint32_t amn = desc_lo(sa, ACH);
     const uint32_t id = idesc_bf16(kM, D, false, true);
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
       const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
-      auto op = [&](int slot) { return sdesc_sw128(ops + slot * kChunk + h * 64 + kk * 32, 16, 1024); };
+      auto op = [&](int slot) { return op_lo(ops, slot, h, kk); };
       if (kQ) {
-        mma_ss(tb + A_U1, op(O_DS), stage_mndesc(sa, ACH, K_BLK + 1, kk), id, acc0);  // dS UK
-        mma_ss(tb + A_U1, op(O_X), stage_mndesc(sa, ACH, K_BLK, kk), id, 1);          // X K
-        mma_ss(tb + A_U2, op(O_P), stage_mndesc(sa, ACH, K_BLK, kk), id, acc0);       // P K
-        mma_ss(tb + A_W, op(O_DS), stage_mndesc(sa, ACH, K_BLK, kk), id, acc0);       // dS K
+        mma_ss_w(tb + A_U1, op(O_DS), mn_lo(amn, K_BLK + 1, kk), id, acc0);  // dS UK
+        mma_ss_w(tb + A_U1, op(O_X), mn_lo(amn, K_BLK, kk), id, 1);          // X K
+        mma_ss_w(tb + A_U2, op(O_P), mn_lo(amn, K_BLK, kk), id, acc0);       // P K
+        mma_ss_w(tb + A_W, op(O_DS), mn_lo(amn, K_BLK, kk), id, acc0);       // dS K
       }
       if (kDo) {
         if (TS) {
           const uint32_t a = ops + h * OP_HALF + kk * 8;
-          mma_ts(tb + A_Y, a, stage_mndesc(sa, ACH, V_BLK + 1, kk), id, acc0);        // P UV
-          mma_ts(tb + A_Y, a + 16, stage_mndesc(sa, ACH, V_BLK, kk), id, 1);          // PB V
+          mma_ts_w(tb + A_Y, a, mn_lo(amn, V_BLK + 1, kk), id, acc0);        // P UV
+          mma_ts_w(tb + A_Y, a + 16, mn_lo(amn, V_BLK, kk), id, 1);          // PB V
         } else {
-          mma_ss(tb + A_Y, op(O_P), stage_mndesc(sa, ACH, V_BLK + 1, kk), id, acc0);  // P UV
-          mma_ss(tb + A_Y, op(O_PB), stage_mndesc(sa, ACH, V_BLK, kk), id, 1);        // PB V
+          mma_ss_w(tb + A_Y, op(O_P), mn_lo(amn, V_BLK + 1, kk), id, acc0);  // P UV
+          mma_ss_w(tb + A_Y, op(O_PB), mn_lo(amn, V_BLK, kk), id, 1);        // PB V
         }
       }
     }
@@ -333,26 +334,27 @@ struct Pass2 {
     const uint32_t i64 = idesc_bf16(kM, 64, false, false), i32 = idesc_bf16(kM, 32, false, false);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k)  // [S^T | K UQ^T] = K [Q; UQ]^T
-      mma_ss(sc, res_desc(res, 0, DC, k), stage_kdesc(sa, ACH, 0, k), i64, k > 0);
+      mma_ss_w(sc, res_lo(res, 0, DC, k), kmaj_lo(sa, ACH, 0, k), i64, k > 0);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k)  // B^T += UK Q^T
-      mma_ss(sc + 32, res_desc(res, 2, DC, k), stage_kdesc(sa, ACH, 0, k), i32, 1);
+      mma_ss_w(sc + 32, res_lo(res, 2, DC, k), kmaj_lo(sa, ACH, 0, k), i32, 1);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-      mma_ss(sc + 64, res_desc(res, 1, DC, k), stage_kdesc(sa, ACH, 2, k), i32, k > 0);  // dP^T = V dO^T
-      mma_ss(sc + 96, res_desc(res, 3, DC, k), stage_kdesc(sa, ACH, 2, k), i32, k > 0);  // C^T = UV dO^T
+      mma_ss_w(sc + 64, res_lo(res, 1, DC, k), kmaj_lo(sa, ACH, 2, k), i32, k > 0);  // dP^T = V dO^T
+      mma_ss_w(sc + 96, res_lo(res, 3, DC, k), kmaj_lo(sa, ACH, 2, k), i32, k > 0);  // C^T = UV dO^T
     }
   }
 
   __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
+    const uint32_t amn = desc_lo(sa, ACH);
     const uint32_t id = idesc_bf16(kM, D, false, true);
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
       const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
       const uint32_t a = ops + h * OP_HALF + kk * 8;
-      mma_ts(tb + A_K, a, stage_mndesc(sa, ACH, 1, kk), id, acc0);        // dS^T UQ
-      mma_ts(tb + A_K, a + 16, stage_mndesc(sa, ACH, 0, kk), id, 1);      // Gs^T Q
-      mma_ts(tb + A_V, a + 32, stage_mndesc(sa, ACH, 2, kk), id, acc0);   // Gdp^T dO
+      mma_ts_w(tb + A_K, a, mn_lo(amn, 1, kk), id, acc0);        // dS^T UQ
+      mma_ts_w(tb + A_K, a + 16, mn_lo(amn, 0, kk), id, 1);      // Gs^T Q
+      mma_ts_w(tb + A_V, a + 32, mn_lo(amn, 2, kk), id, acc0);   // Gdp^T dO
     }
   }
 

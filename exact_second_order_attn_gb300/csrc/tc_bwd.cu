@@ -76,15 +76,16 @@ struct DqOp {
     const uint32_t i32 = idesc_bf16(tile::kM, 32, false, false);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-      mma_ss(sc, tile::res_desc(res, 0, DC, k), tile::stage_kdesc(sa, ACH, 0, k), i32, k > 0);       // S
-      mma_ss(sc + 32, tile::res_desc(res, 1, DC, k), tile::stage_kdesc(sb, BCH, 0, k), i32, k > 0);  // dP
+      mma_ss_w(sc, tile::res_lo(res, 0, DC, k), tile::kmaj_lo(sa, ACH, 0, k), i32, k > 0);       // S
+      mma_ss_w(sc + 32, tile::res_lo(res, 1, DC, k), tile::kmaj_lo(sb, BCH, 0, k), i32, k > 0);  // dP
     }
   }
   __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
+    const uint32_t amn = desc_lo(sa, ACH);
     const uint32_t id = idesc_bf16(tile::kM, D, false, true);
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk)
-      mma_ts(tb, ops + h * OP_HALF + kk * 8, tile::stage_mndesc(sa, ACH, 0, kk), id,
+      mma_ts_w(tb, ops + h * OP_HALF + kk * 8, tile::mn_lo(amn, 0, kk), id,
              (first && kk == 0) ? 0u : 1u);  // dQ += dS K
   }
   struct Row {
@@ -200,18 +201,19 @@ struct DkvOp {
     const uint32_t i32 = idesc_bf16(tile::kM, 32, false, false);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-      mma_ss(sc, tile::res_desc(res, 0, DC, k), tile::stage_kdesc(sa, ACH, 0, k), i32, k > 0);       // S^T
-      mma_ss(sc + 32, tile::res_desc(res, 1, DC, k), tile::stage_kdesc(sa, ACH, 1, k), i32, k > 0);  // dP^T
+      mma_ss_w(sc, tile::res_lo(res, 0, DC, k), tile::kmaj_lo(sa, ACH, 0, k), i32, k > 0);       // S^T
+      mma_ss_w(sc + 32, tile::res_lo(res, 1, DC, k), tile::kmaj_lo(sa, ACH, 1, k), i32, k > 0);  // dP^T
     }
   }
   __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
+    const uint32_t amn = desc_lo(sa, ACH);
     const uint32_t id = idesc_bf16(tile::kM, D, false, true);
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
       const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
       const uint32_t a = ops + h * OP_HALF + kk * 8;
-      mma_ts(tb + D, a, tile::stage_mndesc(sa, ACH, 1, kk), id, acc0);   // dV += P^T dO
-      mma_ts(tb, a + 16, tile::stage_mndesc(sa, ACH, 0, kk), id, acc0);  // dK += dS^T Q
+      mma_ts_w(tb + D, a, tile::mn_lo(amn, 1, kk), id, acc0);   // dV += P^T dO
+      mma_ts_w(tb, a + 16, tile::mn_lo(amn, 0, kk), id, acc0);  // dK += dS^T Q
     }
   }
   struct Row {};

@@ -151,46 +151,46 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd2_tc(const __grid_constan
   } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA
     // S(t) for both blocks, and P V per block, each issued in order; the
-    // thread issues whatever is ready (P V first), probing without blocking.
-    if (live && (tid & 31) == 0) {
-      const uint32_t res_a = smem_u32(res), st_a = smem_u32(stages);
+    // warp issues whatever is ready (P V first), probing without blocking.
+    if (live) {  // the whole warp runs the loop; lane 0 issues (elect.sync)
+      const uint32_t res_l = desc_lo(smem_u32(res), 16), st_a = smem_u32(stages);
       const uint32_t i32 = idesc_bf16(kM, 32, false, false);
       const uint32_t id = idesc_bf16(kM, D, false, true);
-      bool ok = mbar_wait(&ctrl.res_full, 0, wt);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.res_full, 0, wt));
       int ns = 0, na[2] = {0, nblk > 1 ? 0 : nt};
       uint64_t idle_since = 0;
       while (ok && (na[0] < nt || na[1] < nt)) {
         bool progressed = false;
         for (int x = 0; x < nblk; ++x) {
           const int u = na[x];
-          if (u < ns && mbar_test(&ctrl.o_full[x][u & 1], (u >> 1) & 1)) {
+          if (u < ns && mbar_test_w(&ctrl.o_full[x][u & 1], (u >> 1) & 1)) {
             tc_fence_after();
-            const uint32_t sb = st_a + (u % kNS) * C::STAGE;
+            const uint32_t vmn = desc_lo(st_a + (u % kNS) * C::STAGE, C::CH);
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk)
-              mma_ts(tb + x * D, tb + C::P_COL + x * 32 + (u & 1) * 16 + kk * 8,
-                     tile::stage_mndesc(sb, C::CH, 1, kk), id, (u == 0 && kk == 0) ? 0u : 1u);
-            mma_commit(&ctrl.o_empty[x][u & 1]);
-            mma_commit(&ctrl.st_empty[u % kNS]);
-            if (u + 1 == nt) mma_commit(&ctrl.acc_full[x]);
+              mma_ts_w(tb + x * D, tb + C::P_COL + x * 32 + (u & 1) * 16 + kk * 8, tile::mn_lo(vmn, 1, kk), id,
+                        (u == 0 && kk == 0) ? 0u : 1u);
+            mma_commit_w(&ctrl.o_empty[x][u & 1]);
+            mma_commit_w(&ctrl.st_empty[u % kNS]);
+            if (u + 1 == nt) mma_commit_w(&ctrl.acc_full[x]);
             na[x] = u + 1;
             progressed = true;
           }
         }
         if (ns < nt) {
           const int t = ns;
-          bool ready = mbar_test(&ctrl.st_full[t % kNS], (t / kNS) & 1);
+          bool ready = mbar_test_w(&ctrl.st_full[t % kNS], (t / kNS) & 1);
           if (ready && t >= 2)
-            for (int x = 0; x < nblk; ++x) ready = ready && mbar_test(&ctrl.s_empty[x][t & 1], ((t - 2) >> 1) & 1);
+            for (int x = 0; x < nblk; ++x) ready = ready && mbar_test_w(&ctrl.s_empty[x][t & 1], ((t - 2) >> 1) & 1);
           if (ready) {
             tc_fence_after();
-            const uint32_t sb = st_a + (t % kNS) * C::STAGE;
+            const uint32_t klo = desc_lo(st_a + (t % kNS) * C::STAGE, 16);
             for (int x = 0; x < nblk; ++x) {
 #pragma unroll
               for (int k = 0; k < D / 16; ++k)
-                mma_ss(tb + C::S_COL + x * 64 + (t & 1) * 32, tile::res_desc(res_a, x, C::DC, k),
-                       tile::stage_kdesc(sb, C::CH, 0, k), i32, k > 0);
-              mma_commit(&ctrl.s_full[x][t & 1]);
+                mma_ss_w(tb + C::S_COL + x * 64 + (t & 1) * 32, tile::res_lo(res_l, x, C::DC, k),
+                          tile::kmaj_lo(klo, C::CH, 0, k), i32, k > 0);
+              mma_commit_w(&ctrl.s_full[x][t & 1]);
             }
             ++ns;
             progressed = true;
@@ -200,19 +200,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd2_tc(const __grid_constan
           idle_since = 0;
         } else {
           __nanosleep(20);
-          const uint64_t now = globaltimer_ns();
+          // lane 0 decides; the decision is broadcast so the warp stays converged
+          const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
+          const int aborting = __shfl_sync(0xffffffffu, *wt.abort, 0);
           if (idle_since == 0) {
             idle_since = now;
-          } else if (*wt.abort) {
+          } else if (aborting) {
             ok = false;
           } else if (now - idle_since > wt.limit) {
-            *wt.abort = 1;
-            atomicOr(p.err, kErrTimeout);
+            if ((tid & 31) == 0) {
+              *wt.abort = 1;
+              atomicOr(p.err, kErrTimeout);
+            }
             ok = false;
           }
         }
       }
-      mma_commit(&ctrl.drain);
+      mma_commit_w(&ctrl.drain);
       mbar_wait_drain(&ctrl.drain, 0, kDrainNs);
     }
   } else {

@@ -226,40 +226,40 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
     // frees stages), so a warpgroup still computing A(u)'s operands does not
     // hold back S(t+1).  Readiness is probed without blocking; one bounded
     // timer covers any stretch without progress.
-    if (live && (tid & 31) == 0) {
-      const uint32_t res_a = smem_u32(res), ra = smem_u32(ring_a), rb = smem_u32(ring_b);
-      const uint32_t ops_a = Op::TS ? (tb + Op::OP_COL) : smem_u32(ops);
-      bool ok = mbar_wait(&ctrl.res_full, 0, wt);
+    if (live) {  // the whole warp runs the loop; lane 0 issues (elect.sync)
+      const uint32_t res_l = desc_lo(smem_u32(res), 16), ra = smem_u32(ring_a), rb = smem_u32(ring_b);
+      const uint32_t ops_a = Op::TS ? (tb + Op::OP_COL) : desc_lo(smem_u32(ops), 16);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.res_full, 0, wt));
       int ns = 0, na = 0;  // next score batch, next accumulator batch
       uint64_t idle_since = 0;
       while (ok && na < nt) {
         bool progressed = false;
-        if (na < ns && mbar_test(&ctrl.o_full[na & 1], (na >> 1) & 1)) {
+        if (na < ns && mbar_test_w(&ctrl.o_full[na & 1], (na >> 1) & 1)) {
           tc_fence_after();
           Op::accum_mmas(tb, ops_a, ra + (na % Op::NSA) * Op::SA, na & 1, na == 0);
-          mma_commit(&ctrl.o_empty[na & 1]);
-          mma_commit(&ctrl.a_empty[na % Op::NSA]);
+          mma_commit_w(&ctrl.o_empty[na & 1]);
+          mma_commit_w(&ctrl.a_empty[na % Op::NSA]);
           ++na;
           progressed = true;
         }
         if (ns < nt) {
           const int t = ns;
-          bool ready = mbar_test(&ctrl.a_full[t % Op::NSA], (t / Op::NSA) & 1);
+          bool ready = mbar_test_w(&ctrl.a_full[t % Op::NSA], (t / Op::NSA) & 1);
           uint32_t stage_b = rb;
           if constexpr (Op::NSB > 0) {
-            ready = ready && mbar_test(&ctrl.b_full[t % Op::NSB], (t / Op::NSB) & 1);
+            ready = ready && mbar_test_w(&ctrl.b_full[t % Op::NSB], (t / Op::NSB) & 1);
             stage_b = rb + (t % Op::NSB) * Op::SB;
           }
           if (ready && t >= Op::NBUF) {  // the previous user of this score buffer has read it
             const int u = t - Op::NBUF;
-            ready = mbar_test(&ctrl.s_empty[u & 1], (u >> 1) & 1);
+            ready = mbar_test_w(&ctrl.s_empty[u & 1], (u >> 1) & 1);
           }
           if (ready) {
             tc_fence_after();
-            Op::score_mmas(tb + Op::ACC + (t % Op::NBUF) * Op::SCOLS, res_a, ra + (t % Op::NSA) * Op::SA,
-                           stage_b);
-            mma_commit(&ctrl.s_full[t & 1]);
-            if constexpr (Op::NSB > 0) mma_commit(&ctrl.b_empty[t % Op::NSB]);
+            Op::score_mmas(tb + Op::ACC + (t % Op::NBUF) * Op::SCOLS, res_l, desc_lo(ra + (t % Op::NSA) * Op::SA, 16),
+                           desc_lo(stage_b, 16));
+            mma_commit_w(&ctrl.s_full[t & 1]);
+            if constexpr (Op::NSB > 0) mma_commit_w(&ctrl.b_empty[t % Op::NSB]);
             ++ns;
             progressed = true;
           }
@@ -268,20 +268,24 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
           idle_since = 0;
         } else {
           __nanosleep(20);
-          const uint64_t now = globaltimer_ns();
+          // lane 0 decides; the decision is broadcast so the warp stays converged
+          const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
+          const int aborting = __shfl_sync(0xffffffffu, *wt.abort, 0);
           if (idle_since == 0) {
             idle_since = now;
-          } else if (*wt.abort) {
+          } else if (aborting) {
             ok = false;
           } else if (now - idle_since > wt.limit) {
-            *wt.abort = 1;
-            atomicOr(p.err, kErrTimeout);
+            if ((tid & 31) == 0) {
+              *wt.abort = 1;
+              atomicOr(p.err, kErrTimeout);
+            }
             ok = false;
           }
         }
       }
-      if (ok) mma_commit(&ctrl.acc_full);
-      mma_commit(&ctrl.drain);
+      if (ok) mma_commit_w(&ctrl.acc_full);
+      mma_commit_w(&ctrl.drain);
       mbar_wait_drain(&ctrl.drain, 0, kDrainNs);
     }
   } else {
@@ -326,22 +330,25 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
 // helpers shared by the policies
 // ---------------------------------------------------------------------------
 
-// K-major operand descriptor of a resident tile (slot, 64-column chunks of
-// 16 KB), k-th 16-column step.
-__device__ __forceinline__ uint64_t res_desc(uint32_t res, int slot, int dc, int k) {
-  return sdesc_sw128(res + (uint32_t)((slot * dc + (k >> 2)) * kChunk + (k & 3) * 32), 16, 1024);
+// Descriptor low words (see tc_ptx.cuh desc_lo).  Offsets are in bytes and
+// compile-time constants once the k loops are unrolled, so each operand of an
+// MMA costs one add.
+// K-major resident tile: slot of `dc` 64-column chunks of 16 KB, k-th 16-column step.
+__device__ __forceinline__ uint32_t res_lo(uint32_t res_lo0, int slot, int dc, int k) {
+  return res_lo0 + (uint32_t)(((slot * dc + (k >> 2)) * kChunk + (k & 3) * 32) >> 4);
 }
-
-// K-major descriptor of a streamed stage whose chunks are `chunk` bytes
-// apart, starting at 32-row block `blk`, k-th 16-column step.
-__device__ __forceinline__ uint64_t stage_kdesc(uint32_t st, int chunk, int blk, int k) {
-  return sdesc_sw128(st + (uint32_t)((k >> 2) * chunk + blk * kBlk + (k & 3) * 32), 16, 1024);
+// K-major streamed stage with 64-column chunks `chunk` bytes apart, 32-row block `blk`.
+__device__ __forceinline__ uint32_t kmaj_lo(uint32_t st_lo0, int chunk, int blk, int k) {
+  return st_lo0 + (uint32_t)(((k >> 2) * chunk + blk * kBlk + (k & 3) * 32) >> 4);
 }
-
-// MN-major descriptor of a streamed 32-row block (rows = K dimension of the
-// MMA) for the kk-th 16-row step; its 64-column chunks are `chunk` bytes apart.
-__device__ __forceinline__ uint64_t stage_mndesc(uint32_t st, int chunk, int blk, int kk) {
-  return sdesc_sw128(st + (uint32_t)(blk * kBlk + kk * 2048), (uint32_t)chunk, 1024);
+// MN-major streamed 32-row block `blk` (rows = the MMA's K), kk-th 16-row step;
+// st_mn_lo0 = desc_lo(stage address, chunk stride).
+__device__ __forceinline__ uint32_t mn_lo(uint32_t st_mn_lo0, int blk, int kk) {
+  return st_mn_lo0 + (uint32_t)((blk * kBlk + kk * 2048) >> 4);
+}
+// K-major operand tile `slot` ([128][64], 16 KB each), half h, kk-th 16-column step.
+__device__ __forceinline__ uint32_t op_lo(uint32_t ops_lo0, int slot, uint32_t h, int kk) {
+  return ops_lo0 + (uint32_t)((slot * kChunk + kk * 32) >> 4) + h * 4u;
 }
 
 // Write 32 packed bf16 (16 words) of row r into columns [32h, 32h+32) of a
