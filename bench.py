@@ -40,11 +40,12 @@ FLOPS_FWD, FLOPS_BWD, FLOPS_BOB = 4, 10, 38   # x N^2 d per head
 DEFAULT_WORKLOAD = "wide_head_b2h16_n16384_d128"
 # Counted GEMMs (2 N^2 d FLOPs each, per head) attributed to each kernel: the
 # 38 N^2 d of BoB = pass 1 (11: S, dP, C, B x2, U1 x2, U2, W, Y x2) + pass 2
-# (8); at d=128 pass 1 runs as a Q-side kernel (9) and a dO-side kernel (Y: 2;
-# its recomputed S and B are not counted).  Forward 2 (S, PV); first backward
+# (8).  Pass 1 runs as three sweeps: U1 (the five score GEMMs + U1 x2 = 7),
+# Z (one GEMM doing the work of U2 and W: 2) and Y (2); the recomputed S, dP
+# and B of the last two are not counted.  Forward 2 (S, PV); first backward
 # 5 (S, dP, dQ in the row kernel, dV, dK in the column kernel; the column
 # kernel's recomputed S and dP are not counted).
-COUNTED_GEMMS = {"bob_pass1": 11, "bob_pass1_qside": 9, "bob_pass1_doside": 2, "bob_pass2": 8,
+COUNTED_GEMMS = {"bob_pass1_u1": 7, "bob_pass1_z": 2, "bob_pass1_y": 2, "bob_pass2": 8,
                  "attn_fwd": 2, "attn_bwd_dq": 3, "attn_bwd_dkdv": 2}
 
 

@@ -19,13 +19,24 @@
 //   b' = B - alpha_i, Gs = P (C + b' t + alpha_i D_i - E_i), Gdp = P b'
 //   gK = tau (dS^T UQ + Gs^T Q), gV = Gdp^T dO
 //
-// TMEM budget (512 columns x 128 lanes fp32).  d=64 pass 1 holds all four
-// accumulators (4 x 64) and two score buffers ([S|B|dP|C], 128 columns each).
-// At d=128 the four accumulators alone fill TMEM, so pass 1 runs as two CTA
-// kinds over the same row blocks: the Q side (U1, U2, W = 384 columns + one
-// score buffer) writes gQ and alpha/E; the dO side (Y) recomputes S and B and
-// writes gdO, with its P / PB operands in TMEM.  Pass 2 keeps gK, gV (2d
-// columns), its score buffer(s) and its three operands (dS, Gs, Gdp) in TMEM.
+// The identity the pass-1 split rests on: with the row totals alpha and EX
+// known, EX U2 + alpha W = sum_j (EX P + alpha dS) K_j, so
+//   gQ = tau (U1 - Z),  Z = sum_j G K_j,  G = EX P + alpha dS.
+//
+// Every score MMA reads its resident operand (Q, UQ, dO in pass 1; K, UK and,
+// at d = 64, V, UV in pass 2) from TMEM, so only the streamed 32-row tile is
+// read from shared memory.  TMEM (512 columns x 128 lanes fp32) then holds
+// one accumulator set per kernel, so pass 1 runs as three kernels over the
+// same 128-row blocks, in stream order:
+//   U1 kernel  U1 (d) | [S|B|dP|C] | (dS, X) halves | Q, UQ, dO
+//              writes U1 into gQ and (alpha, E) into the workspace;
+//   Z kernel   Z (d) | [S|dP] x 2 | G halves | Q, dO
+//              reads (alpha, E) and U1, writes gQ = tau (U1 - Z);
+//   Y kernel   Y (d) | [S|B] x 2 | (P, PB) halves | Q, UQ
+//              writes gdO = Y - alpha O (alpha summed again from P B).
+// Pass 2: gK, gV (2d) | [S|B|dP|C] | then, at d = 64, the (dS, Gs, Gdp)
+// halves and K, UK, V, UV; at d = 128, K and UK (V, UV stay in shared memory
+// and the three operands go to shared memory).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -41,11 +52,11 @@ namespace {
 using namespace tc;
 using namespace tile;
 
-enum Role { kBoth = 0, kQSide = 1, kDoSide = 2 };
+enum Role { kU1 = 0, kZ = 1, kY = 2 };
 
 struct P1Params {
-  CUtensorMap mQ, mdO, mUQ;        // resident, box {64, 128}
-  CUtensorMap mK, mUK, mV, mUV;    // streamed, box {64, 32}
+  CUtensorMap mK, mUK, mV, mUV;              // streamed, box {64, 32}
+  const __nv_bfloat16 *Q, *UQ, *dO;          // resident (copied into TMEM)
   const float *L, *D, *O;
   float *gQ, *gdO, *ws;
   int N;
@@ -56,8 +67,9 @@ struct P1Params {
 };
 
 struct P2Params {
-  CUtensorMap mK, mV, mUK, mUV;    // resident, box {64, 128}
-  CUtensorMap mQ, mUQ, mdO;        // streamed, box {64, 32}
+  CUtensorMap mV, mUV;                       // resident in shared memory at d = 128, box {64, 128}
+  CUtensorMap mQ, mUQ, mdO;                  // streamed, box {64, 32}
+  const __nv_bfloat16 *K, *UK, *V, *UV;      // resident (copied into TMEM)
   const float *L, *D, *ws;
   float *gK, *gV;
   int N;
@@ -74,82 +86,76 @@ template <int D_, int ROLE>
 struct Pass1 {
   using Params = P1Params;
   static constexpr int D = D_, DC = D / 64;
-  static constexpr bool kQ = ROLE != kDoSide;   // gQ, alpha, E
-  static constexpr bool kDo = ROLE != kQSide;   // gdO
-  // resident slots: Q, UQ, dO
-  static constexpr int NRES = kQ ? 3 : 2;
-  static constexpr int RES = NRES * DC * kChunk;
+  static constexpr int RES = 0;
+  static constexpr int TRES = ROLE == kU1 ? 3 : 2;   // U1: Q UQ dO;  Z: Q dO;  Y: Q UQ
   // ring A holds what the accumulator MMAs read, ring B what only the score
-  // MMAs read:  both: A = [K UK V UV];  Q side: A = [K UK], B = [V UV];
-  // dO side: A = [V UV], B = [K UK]
-  static constexpr int ABLK = ROLE == kBoth ? 4 : 2, BBLK = ROLE == kBoth ? 0 : 2;
+  // MMAs read:  U1: A = [K UK], B = [V UV];  Z: A = K, B = V;  Y: A = [V UV], B = [K UK]
+  static constexpr int ABLK = ROLE == kZ ? 1 : 2, BBLK = ABLK;
   static constexpr int ACH = ABLK * kBlk, BCH = BBLK * kBlk;
   static constexpr int SA = DC * ACH, SB = DC * BCH, SA_TX = SA, SB_TX = SB;
-  static constexpr int NSA = ROLE == kQSide ? 3 : 4;
-  static constexpr int NSB = ROLE == kBoth ? 0 : (ROLE == kQSide ? 2 : 4);
+  static constexpr int NSA = (D == 128 && ROLE != kZ) ? 6 : 8, NSB = NSA;
   static constexpr bool VEC = false;
   static constexpr int VEC_OFF = 0;
-  static constexpr bool ROW_SUMS = true;
-  static constexpr bool TS = ROLE == kDoSide;
-  static constexpr int NOPS = TS ? 0 : 1 + (kQ ? 2 : 0) + (kDo ? 1 : 0);  // P, dS, X, PB tiles
-  static constexpr int OPS = NOPS * kChunk;
-  static constexpr int ACC = ((kQ ? 3 : 0) + (kDo ? 1 : 0)) * D;
-  static constexpr int SCOLS = kQ ? 128 : 64;    // [S|B|dP|C] or [S|B]
-  static constexpr int NBUF = ROLE == kQSide ? 1 : 2;
-  static constexpr int OP_HALF = 32;             // TS: P, PB (16 columns each)
+  static constexpr bool ROW_SUMS = ROLE != kZ;
+  static constexpr bool TS = true;
+  static constexpr int OPS = 0;
+  static constexpr int ACC = D;
+  static constexpr int SCOLS = ROLE == kU1 ? 128 : 64;   // [S|B|dP|C], [S|dP] or [S|B]
+  static constexpr int NBUF = (ROLE == kU1 && D == 128) ? 1 : 2;
+  static constexpr int OP_HALF = ROLE == kZ ? 16 : 32;   // (dS, X), G or (P, PB)
   static constexpr int OP_COL = ACC + NBUF * SCOLS;
-  static constexpr int SMEM = RES + NSA * SA + NSB * SB + OPS;
-  static_assert(OP_COL + (TS ? 2 * OP_HALF : 0) <= 512, "TMEM budget");
+  static constexpr int TRES_COL = OP_COL + 2 * OP_HALF;
+  static constexpr int SMEM = NSA * SA + NSB * SB;
+  static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
   static_assert(SMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
   static_assert(NSA <= kMaxStages && NSB <= kMaxStages, "stage count");
-  // where K, UK (= K block + 1) and V, UV (= V block + 1) live
-  static constexpr bool K_IN_B = ROLE == kDoSide, V_IN_B = ROLE == kQSide;
-  static constexpr int K_BLK = 0, V_BLK = ROLE == kBoth ? 2 : 0;
-  static constexpr int A_U1 = 0, A_U2 = D, A_W = 2 * D, A_Y = kQ ? 3 * D : 0;
-  static constexpr int O_P = 0, O_DS = 1, O_X = 2, O_PB = kQ ? 3 : 1;
 
-  __device__ static void load_res(const Params& p, uint8_t* res, uint64_t* bar, int row0, int head) {
-    const CUtensorMap* m[3] = {&p.mQ, &p.mUQ, &p.mdO};
-    for (int s = 0; s < NRES; ++s)
-      for (int kc = 0; kc < DC; ++kc) tma_load_3d(res + (s * DC + kc) * kChunk, m[s], bar, kc * 64, row0, head);
+  __device__ static const void* tres_src(const Params& p, int s) {
+    if (ROLE == kU1) return s == 0 ? (const void*)p.Q : s == 1 ? (const void*)p.UQ : (const void*)p.dO;
+    if (ROLE == kZ) return s == 0 ? (const void*)p.Q : (const void*)p.dO;
+    return s == 0 ? (const void*)p.Q : (const void*)p.UQ;
+  }
+  __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
+  __device__ static void load_pair(const CUtensorMap* m0, const CUtensorMap* m1, uint8_t* st, int ch, uint64_t* bar,
+                                   int t, int head) {
+    for (int kc = 0; kc < DC; ++kc) {
+      tma_load_3d(st + kc * ch, m0, bar, kc * 64, t * kT, head);
+      if (m1) tma_load_3d(st + kc * ch + kBlk, m1, bar, kc * 64, t * kT, head);
+    }
   }
   __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
-    for (int kc = 0; kc < DC; ++kc) {
-      uint8_t* c = st + kc * ACH;
-      if (ROLE == kBoth || ROLE == kQSide) {
-        tma_load_3d(c, &p.mK, bar, kc * 64, t * kT, head);
-        tma_load_3d(c + kBlk, &p.mUK, bar, kc * 64, t * kT, head);
-      }
-      if (ROLE == kBoth || ROLE == kDoSide) {
-        uint8_t* v = c + V_BLK * kBlk;
-        tma_load_3d(v, &p.mV, bar, kc * 64, t * kT, head);
-        tma_load_3d(v + kBlk, &p.mUV, bar, kc * 64, t * kT, head);
-      }
-    }
+    if (ROLE == kU1) load_pair(&p.mK, &p.mUK, st, ACH, bar, t, head);
+    if (ROLE == kZ) load_pair(&p.mK, nullptr, st, ACH, bar, t, head);
+    if (ROLE == kY) load_pair(&p.mV, &p.mUV, st, ACH, bar, t, head);
   }
   __device__ static void load_b(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
-    const CUtensorMap* m0 = ROLE == kQSide ? &p.mV : &p.mK;
-    const CUtensorMap* m1 = ROLE == kQSide ? &p.mUV : &p.mUK;
-    for (int kc = 0; kc < DC; ++kc) {
-      tma_load_3d(st + kc * BCH, m0, bar, kc * 64, t * kT, head);
-      tma_load_3d(st + kc * BCH + kBlk, m1, bar, kc * 64, t * kT, head);
-    }
+    if (ROLE == kU1) load_pair(&p.mV, &p.mUV, st, BCH, bar, t, head);
+    if (ROLE == kZ) load_pair(&p.mV, nullptr, st, BCH, bar, t, head);
+    if (ROLE == kY) load_pair(&p.mK, &p.mUK, st, BCH, bar, t, head);
   }
 
-  __device__ static void score_mmas(uint32_t sc, uint32_t res, uint32_t sa, uint32_t sb) {
-    const uint32_t kst = K_IN_B ? sb : sa, vst = V_IN_B ? sb : sa;
-    const int kch = K_IN_B ? BCH : ACH, vch = V_IN_B ? BCH : ACH;
+  __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t, uint32_t sa, uint32_t sb) {
     const uint32_t i64 = idesc_bf16(kM, 64, false, false), i32 = idesc_bf16(kM, 32, false, false);
+    if (ROLE == kZ) {
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        mma_ts_w(sc, tres_a(tres, 0, D, k), kmaj_lo(sa, ACH, 0, k), i32, k > 0);       // S = Q K^T
+        mma_ts_w(sc + 32, tres_a(tres, 1, D, k), kmaj_lo(sb, BCH, 0, k), i32, k > 0);  // dP = dO V^T
+      }
+      return;
+    }
+    const uint32_t kst = ROLE == kU1 ? sa : sb;   // the [K | UK] tile
+    const int kch = ROLE == kU1 ? ACH : BCH;
 #pragma unroll
     for (int k = 0; k < D / 16; ++k)  // [S | Q UK^T] = Q [K; UK]^T
-      mma_ss_w(sc, res_lo(res, 0, DC, k), kmaj_lo(kst, kch, K_BLK, k), i64, k > 0);
+      mma_ts_w(sc, tres_a(tres, 0, D, k), kmaj_lo(kst, kch, 0, k), i64, k > 0);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k)  // B += UQ K^T
-      mma_ss_w(sc + 32, res_lo(res, 1, DC, k), kmaj_lo(kst, kch, K_BLK, k), i32, 1);
-    if (kQ) {
+      mma_ts_w(sc + 32, tres_a(tres, 1, D, k), kmaj_lo(kst, kch, 0, k), i32, 1);
+    if (ROLE == kU1) {
 #pragma unroll
       for (int k = 0; k < D / 16; ++k)  // [dP | C] = dO [V; UV]^T
-        mma_ss_w(sc + 64, res_lo(res, 2, DC, k), kmaj_lo(vst, vch, V_BLK, k), i64, k > 0);
+        mma_ts_w(sc + 64, tres_a(tres, 2, D, k), kmaj_lo(sb, BCH, 0, k), i64, k > 0);
     }
   }
 
@@ -159,22 +165,15 @@ struct Pass1 {
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
       const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
-      auto op = [&](int slot) { return op_lo(ops, slot, h, kk); };
-      if (kQ) {
-        mma_ss_w(tb + A_U1, op(O_DS), mn_lo(amn, K_BLK + 1, kk), id, acc0);  // dS UK
-        mma_ss_w(tb + A_U1, op(O_X), mn_lo(amn, K_BLK, kk), id, 1);          // X K
-        mma_ss_w(tb + A_U2, op(O_P), mn_lo(amn, K_BLK, kk), id, acc0);       // P K
-        mma_ss_w(tb + A_W, op(O_DS), mn_lo(amn, K_BLK, kk), id, acc0);       // dS K
-      }
-      if (kDo) {
-        if (TS) {
-          const uint32_t a = ops + h * OP_HALF + kk * 8;
-          mma_ts_w(tb + A_Y, a, mn_lo(amn, V_BLK + 1, kk), id, acc0);        // P UV
-          mma_ts_w(tb + A_Y, a + 16, mn_lo(amn, V_BLK, kk), id, 1);          // PB V
-        } else {
-          mma_ss_w(tb + A_Y, op(O_P), mn_lo(amn, V_BLK + 1, kk), id, acc0);  // P UV
-          mma_ss_w(tb + A_Y, op(O_PB), mn_lo(amn, V_BLK, kk), id, 1);        // PB V
-        }
+      const uint32_t a = ops + h * OP_HALF + kk * 8;
+      if (ROLE == kU1) {
+        mma_ts_w(tb, a, mn_lo(amn, 1, kk), id, acc0);   // U1 += dS UK
+        mma_ts_w(tb, a + 16, mn_lo(amn, 0, kk), id, 1);  // U1 += X K
+      } else if (ROLE == kZ) {
+        mma_ts_w(tb, a, mn_lo(amn, 0, kk), id, acc0);   // Z += G K
+      } else {
+        mma_ts_w(tb, a, mn_lo(amn, 1, kk), id, acc0);   // Y += P UV
+        mma_ts_w(tb, a + 16, mn_lo(amn, 0, kk), id, 1);  // Y += PB V
       }
     }
   }
@@ -188,98 +187,88 @@ struct Pass1 {
     w.Di = p.D[vo];
     w.alpha = 0.f;
     w.ex = 0.f;
+    if (ROLE == kZ) {  // row totals of the U1 kernel; EX = E - D alpha
+      w.alpha = p.ws[2 * vo];
+      w.ex = fmaf(-w.Di, w.alpha, p.ws[2 * vo + 1]);
+    }
   }
 
-  __device__ static bool ew_tile(Row& w, const Params& p, const TileArgs& a, const TileSync& s, int r) {
+  __device__ static bool ew_tile(Row& w, const Params& p, const TileArgs& a, const TileSync& s, int) {
     const float sc = p.tau * kLog2e;
-    uint32_t wP[16], wdS[16], wX[16], wPB[16];
+    uint32_t w0[16], w1[16];
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      float S[16], B[16], dP[16], C[16];
-      if (kQ)
-        tmem_ld16x4(a.sc + q * 16, a.sc + 32 + q * 16, a.sc + 64 + q * 16, a.sc + 96 + q * 16, S, B, dP, C);
+      float S[16], X1[16], dP[16], C[16];   // X1 = B (U1, Y) or dP (Z)
+      if (ROLE == kU1)
+        tmem_ld16x4(a.sc + q * 16, a.sc + 32 + q * 16, a.sc + 64 + q * 16, a.sc + 96 + q * 16, S, X1, dP, C);
       else
-        tmem_ld16x2(a.sc + q * 16, a.sc + 32 + q * 16, S, B);
+        tmem_ld16x2(a.sc + q * 16, a.sc + 32 + q * 16, S, X1);
       if (q == 1) s.release_scores();
 #pragma unroll
       for (int j = 0; j < 16; j += 2) {
-        float pv[2], dsv[2], xv[2], pbv[2];
+        float v0[2], v1[2] = {0.f, 0.f};
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const float pe = ex2(fmaf(S[j + e], sc, w.nL));
-          const float be = p.tau * B[j + e];
-          pv[e] = pe;
-          pbv[e] = pe * be;
-          w.alpha += pbv[e];
-          if (kQ) {
-            const float te = dP[j + e] - w.Di;
-            dsv[e] = pe * te;
-            xv[e] = pe * fmaf(be, te, C[j + e]);
-            w.ex += xv[e];
+          if (ROLE == kZ) {
+            const float ds = pe * (X1[j + e] - w.Di);
+            v0[e] = fmaf(w.ex, pe, w.alpha * ds);   // G = EX P + alpha dS
+          } else {
+            const float be = p.tau * X1[j + e];
+            const float pb = pe * be;
+            w.alpha += pb;
+            if (ROLE == kU1) {
+              const float te = dP[j + e] - w.Di;
+              v0[e] = pe * te;                        // dS
+              v1[e] = pe * fmaf(be, te, C[j + e]);    // X
+              w.ex += v1[e];
+            } else {
+              v0[e] = pe;                             // P
+              v1[e] = pb;                             // PB
+            }
           }
         }
         const int k = q * 8 + j / 2;
-        wP[k] = pack_bf16x2(pv[0], pv[1]);
-        wPB[k] = pack_bf16x2(pbv[0], pbv[1]);
-        if (kQ) {
-          wdS[k] = pack_bf16x2(dsv[0], dsv[1]);
-          wX[k] = pack_bf16x2(xv[0], xv[1]);
-        }
+        w0[k] = pack_bf16x2(v0[0], v0[1]);
+        w1[k] = pack_bf16x2(v1[0], v1[1]);
       }
     }
     if (!s.acquire_ops()) return false;
-    if (TS) {
-      tmem_st16_nowait(a.ops, wP);
-      tmem_st16_nowait(a.ops + 16, wPB);
-    } else {
-      write_op_half(a.ops + O_P * kChunk, r, a.h, wP);
-      if (kQ) {
-        write_op_half(a.ops + O_DS * kChunk, r, a.h, wdS);
-        write_op_half(a.ops + O_X * kChunk, r, a.h, wX);
-      }
-      if (kDo) write_op_half(a.ops + O_PB * kChunk, r, a.h, wPB);
-    }
+    tmem_st16_nowait(a.ops, w0);
+    if (ROLE != kZ) tmem_st16_nowait(a.ops + 16, w1);
     s.publish_ops();
     return true;
   }
 
   __device__ static void epilogue(Row& w, const Params& p, const EpiArgs& e) {
     float alpha = w.alpha, ex = w.ex;
-    if (!e.sum_rows(alpha, ex)) return;
+    if (ROW_SUMS && !e.sum_rows(alpha, ex)) return;
     const size_t vo = (size_t)e.head * p.N + e.blk0 + e.r;
     const size_t ro = vo * D;
     const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
-    if (kQ) {
 #pragma unroll 1
-      for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
-        float u1[16], u2[16], wv[16], o[16];
-        tmem_ld16x2(e.tm + A_U1 + c0, e.tm + A_U2 + c0, u1, u2);
-        tmem_ld16(e.tm + A_W + c0, wv);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) o[j] = p.tau * (u1[j] - ex * u2[j] - alpha * wv[j]);
-        store16(p.gQ + ro + c0, o);
-      }
-      if (e.g == 0) {
-        p.ws[2 * vo] = alpha;
-        p.ws[2 * vo + 1] = fmaf(w.Di, alpha, ex);
-      }
-    }
-    if (kDo) {
-#pragma unroll 1
-      for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
-        float y[16], o[16];
-        tmem_ld16(e.tm + A_Y + c0, y);
-        const float4* src = reinterpret_cast<const float4*>(p.O + ro + c0);
+    for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+      float acc[16], o[16];
+      tmem_ld16(e.tm + c0, acc);
+      if (ROLE == kU1) {
+        store16(p.gQ + ro + c0, acc);   // U1, finished by the Z kernel
+      } else {
+        const float4* src = reinterpret_cast<const float4*>((ROLE == kZ ? p.gQ : p.O) + ro + c0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float4 v = src[q];
-          o[4 * q] = y[4 * q] - alpha * v.x;
-          o[4 * q + 1] = y[4 * q + 1] - alpha * v.y;
-          o[4 * q + 2] = y[4 * q + 2] - alpha * v.z;
-          o[4 * q + 3] = y[4 * q + 3] - alpha * v.w;
+          const float u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            o[4 * q + i] = ROLE == kZ ? p.tau * (u[i] - acc[4 * q + i])     // gQ = tau (U1 - Z)
+                                      : fmaf(-alpha, u[i], acc[4 * q + i]);  // gdO = Y - alpha O
         }
-        store16(p.gdO + ro + c0, o);
+        store16((ROLE == kZ ? p.gQ : p.gdO) + ro + c0, o);
       }
+    }
+    if (ROLE == kU1 && e.g == 0) {
+      p.ws[2 * vo] = alpha;
+      p.ws[2 * vo + 1] = fmaf(w.Di, alpha, ex);
     }
   }
 };
@@ -291,28 +280,33 @@ template <int D_>
 struct Pass2 {
   using Params = P2Params;
   static constexpr int D = D_, DC = D / 64;
-  static constexpr int NRES = 4;                  // K, V, UK, UV
-  static constexpr int RES = NRES * DC * kChunk;
+  static constexpr bool kAllTmem = D == 64;        // V, UV also in TMEM; operands in TMEM
+  static constexpr int TRES = kAllTmem ? 4 : 2;    // K, UK (, V, UV)
+  static constexpr int RES = kAllTmem ? 0 : 2 * DC * kChunk;   // V, UV in shared memory
   static constexpr int ACH = 3 * kBlk;            // [Q | UQ | dO] per chunk
   static constexpr int VEC_OFF = DC * ACH;        // L (32), D (32), (alpha, E) (64) floats
   static constexpr int SA = DC * ACH + 1024, SA_TX = DC * ACH + 512;
   static constexpr int SB = 0, SB_TX = 0;
-  static constexpr int NSA = D == 128 ? 3 : 4, NSB = 0;
-  static constexpr bool VEC = true, ROW_SUMS = false, TS = true;
-  static constexpr int OPS = 0;
+  static constexpr int NSA = kAllTmem ? 8 : 4, NSB = 0;
+  static constexpr bool VEC = true, ROW_SUMS = false, TS = kAllTmem;
+  static constexpr int OPS = kAllTmem ? 0 : 3 * kChunk;   // dS, Gs, Gdp tiles [128][64]
   static constexpr int ACC = 2 * D;               // gK, gV accumulators
   static constexpr int SCOLS = 128;               // [S|B|dP|C]
-  static constexpr int NBUF = D == 128 ? 1 : 2;
-  static constexpr int OP_HALF = 48;              // dS, Gs, Gdp (16 columns each)
+  static constexpr int NBUF = 1;
+  static constexpr int OP_HALF = 48;              // TMEM operands: dS, Gs, Gdp (16 columns each)
   static constexpr int OP_COL = ACC + NBUF * SCOLS;
-  static constexpr int SMEM = RES + NSA * SA;
-  static_assert(OP_COL + 2 * OP_HALF <= 512, "TMEM budget");
+  static constexpr int TRES_COL = OP_COL + (kAllTmem ? 2 * OP_HALF : 0);
+  static constexpr int SMEM = RES + NSA * SA + OPS;
+  static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
   static_assert(SMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
   static constexpr int A_K = 0, A_V = D;
 
+  __device__ static const void* tres_src(const Params& p, int s) {
+    return s == 0 ? (const void*)p.K : s == 1 ? (const void*)p.UK : s == 2 ? (const void*)p.V : (const void*)p.UV;
+  }
   __device__ static void load_res(const Params& p, uint8_t* res, uint64_t* bar, int col0, int head) {
-    const CUtensorMap* m[4] = {&p.mK, &p.mV, &p.mUK, &p.mUV};
-    for (int s = 0; s < NRES; ++s)
+    const CUtensorMap* m[2] = {&p.mV, &p.mUV};
+    for (int s = 0; s < 2; ++s)
       for (int kc = 0; kc < DC; ++kc) tma_load_3d(res + (s * DC + kc) * kChunk, m[s], bar, kc * 64, col0, head);
   }
   __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
@@ -330,18 +324,23 @@ struct Pass2 {
   }
   __device__ static void load_b(const Params&, uint8_t*, uint64_t*, int, int) {}
 
-  __device__ static void score_mmas(uint32_t sc, uint32_t res, uint32_t sa, uint32_t) {
+  __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t res, uint32_t sa, uint32_t) {
     const uint32_t i64 = idesc_bf16(kM, 64, false, false), i32 = idesc_bf16(kM, 32, false, false);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k)  // [S^T | K UQ^T] = K [Q; UQ]^T
-      mma_ss_w(sc, res_lo(res, 0, DC, k), kmaj_lo(sa, ACH, 0, k), i64, k > 0);
+      mma_ts_w(sc, tres_a(tres, 0, D, k), kmaj_lo(sa, ACH, 0, k), i64, k > 0);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k)  // B^T += UK Q^T
-      mma_ss_w(sc + 32, res_lo(res, 2, DC, k), kmaj_lo(sa, ACH, 0, k), i32, 1);
+      mma_ts_w(sc + 32, tres_a(tres, 1, D, k), kmaj_lo(sa, ACH, 0, k), i32, 1);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-      mma_ss_w(sc + 64, res_lo(res, 1, DC, k), kmaj_lo(sa, ACH, 2, k), i32, k > 0);  // dP^T = V dO^T
-      mma_ss_w(sc + 96, res_lo(res, 3, DC, k), kmaj_lo(sa, ACH, 2, k), i32, k > 0);  // C^T = UV dO^T
+      if (kAllTmem) {
+        mma_ts_w(sc + 64, tres_a(tres, 2, D, k), kmaj_lo(sa, ACH, 2, k), i32, k > 0);  // dP^T = V dO^T
+        mma_ts_w(sc + 96, tres_a(tres, 3, D, k), kmaj_lo(sa, ACH, 2, k), i32, k > 0);  // C^T = UV dO^T
+      } else {
+        mma_ss_w(sc + 64, res_lo(res, 0, DC, k), kmaj_lo(sa, ACH, 2, k), i32, k > 0);
+        mma_ss_w(sc + 96, res_lo(res, 1, DC, k), kmaj_lo(sa, ACH, 2, k), i32, k > 0);
+      }
     }
   }
 
@@ -351,17 +350,23 @@ struct Pass2 {
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
       const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
-      const uint32_t a = ops + h * OP_HALF + kk * 8;
-      mma_ts_w(tb + A_K, a, mn_lo(amn, 1, kk), id, acc0);        // dS^T UQ
-      mma_ts_w(tb + A_K, a + 16, mn_lo(amn, 0, kk), id, 1);      // Gs^T Q
-      mma_ts_w(tb + A_V, a + 32, mn_lo(amn, 2, kk), id, acc0);   // Gdp^T dO
+      if (kAllTmem) {
+        const uint32_t a = ops + h * OP_HALF + kk * 8;
+        mma_ts_w(tb + A_K, a, mn_lo(amn, 1, kk), id, acc0);        // dS^T UQ
+        mma_ts_w(tb + A_K, a + 16, mn_lo(amn, 0, kk), id, 1);      // Gs^T Q
+        mma_ts_w(tb + A_V, a + 32, mn_lo(amn, 2, kk), id, acc0);   // Gdp^T dO
+      } else {
+        mma_ss_w(tb + A_K, op_lo(ops, 0, h, kk), mn_lo(amn, 1, kk), id, acc0);
+        mma_ss_w(tb + A_K, op_lo(ops, 1, h, kk), mn_lo(amn, 0, kk), id, 1);
+        mma_ss_w(tb + A_V, op_lo(ops, 2, h, kk), mn_lo(amn, 2, kk), id, acc0);
+      }
     }
   }
 
   struct Row {};
   __device__ static void ew_init(Row&, const Params&, int, int, int) {}
 
-  __device__ static bool ew_tile(Row&, const Params& p, const TileArgs& a, const TileSync& s, int) {
+  __device__ static bool ew_tile(Row&, const Params& p, const TileArgs& a, const TileSync& s, int r) {
     const float sc = p.tau * kLog2e;
     const float* vL = a.vec;
     const float* vD = a.vec + 32;
@@ -394,9 +399,15 @@ struct Pass2 {
       }
     }
     if (!s.acquire_ops()) return false;
-    tmem_st16_nowait(a.ops, wdS);
-    tmem_st16_nowait(a.ops + 16, wGs);
-    tmem_st16_nowait(a.ops + 32, wGd);
+    if (kAllTmem) {
+      tmem_st16_nowait(a.ops, wdS);
+      tmem_st16_nowait(a.ops + 16, wGs);
+      tmem_st16_nowait(a.ops + 32, wGd);
+    } else {
+      write_op_half(a.ops, r, a.h, wdS);
+      write_op_half(a.ops + kChunk, r, a.h, wGs);
+      write_op_half(a.ops + 2 * kChunk, r, a.h, wGd);
+    }
     s.publish_ops();
     return true;
   }
@@ -434,11 +445,12 @@ template <int D>
 cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   P1Params p1;
   const int BH = a.BH, N = a.N;
-  bool ok = make_bf16_map(&p1.mQ, a.Q, BH, N, D, kM) && make_bf16_map(&p1.mdO, a.dO, BH, N, D, kM) &&
-            make_bf16_map(&p1.mUQ, a.UQ, BH, N, D, kM) && make_bf16_map(&p1.mK, a.K, BH, N, D, kT) &&
-            make_bf16_map(&p1.mUK, a.UK, BH, N, D, kT) && make_bf16_map(&p1.mV, a.V, BH, N, D, kT) &&
-            make_bf16_map(&p1.mUV, a.UV, BH, N, D, kT);
+  bool ok = make_bf16_map(&p1.mK, a.K, BH, N, D, kT) && make_bf16_map(&p1.mUK, a.UK, BH, N, D, kT) &&
+            make_bf16_map(&p1.mV, a.V, BH, N, D, kT) && make_bf16_map(&p1.mUV, a.UV, BH, N, D, kT);
   if (!ok) return cudaErrorInvalidValue;
+  p1.Q = static_cast<const __nv_bfloat16*>(a.Q);
+  p1.UQ = static_cast<const __nv_bfloat16*>(a.UQ);
+  p1.dO = static_cast<const __nv_bfloat16*>(a.dO);
   p1.L = a.L;
   p1.D = a.D;
   p1.O = a.O;
@@ -451,20 +463,20 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   p1.wait_ns = c.wait_ns;
   p1.stall = c.stall;
   const dim3 grid(N / kM, BH);
-  cudaError_t e;
-  if constexpr (D == 64) {
-    e = launch<Pass1<D, kBoth>>("bob_pass1", p1, grid, s);
-  } else {
-    e = launch<Pass1<D, kQSide>>("bob_pass1_qside", p1, grid, s);
-    if (e == cudaSuccess) e = launch<Pass1<D, kDoSide>>("bob_pass1_doside", p1, grid, s);
-  }
+  // the Z kernel reads what the U1 kernel wrote (U1 in gQ, alpha and E)
+  cudaError_t e = launch<Pass1<D, kU1>>("bob_pass1_u1", p1, grid, s);
+  if (e == cudaSuccess) e = launch<Pass1<D, kZ>>("bob_pass1_z", p1, grid, s);
+  if (e == cudaSuccess) e = launch<Pass1<D, kY>>("bob_pass1_y", p1, grid, s);
   if (e != cudaSuccess) return e;
   P2Params p2;
-  ok = make_bf16_map(&p2.mK, a.K, BH, N, D, kM) && make_bf16_map(&p2.mV, a.V, BH, N, D, kM) &&
-       make_bf16_map(&p2.mUK, a.UK, BH, N, D, kM) && make_bf16_map(&p2.mUV, a.UV, BH, N, D, kM) &&
-       make_bf16_map(&p2.mQ, a.Q, BH, N, D, kT) && make_bf16_map(&p2.mUQ, a.UQ, BH, N, D, kT) &&
-       make_bf16_map(&p2.mdO, a.dO, BH, N, D, kT);
+  ok = make_bf16_map(&p2.mQ, a.Q, BH, N, D, kT) && make_bf16_map(&p2.mUQ, a.UQ, BH, N, D, kT) &&
+       make_bf16_map(&p2.mdO, a.dO, BH, N, D, kT) && make_bf16_map(&p2.mV, a.V, BH, N, D, kM) &&
+       make_bf16_map(&p2.mUV, a.UV, BH, N, D, kM);
   if (!ok) return cudaErrorInvalidValue;
+  p2.K = static_cast<const __nv_bfloat16*>(a.K);
+  p2.UK = static_cast<const __nv_bfloat16*>(a.UK);
+  p2.V = static_cast<const __nv_bfloat16*>(a.V);
+  p2.UV = static_cast<const __nv_bfloat16*>(a.UV);
   p2.L = a.L;
   p2.D = a.D;
   p2.ws = a.ws;
@@ -485,3 +497,7 @@ cudaError_t tc_bob(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
 }
 
 }  // namespace fbob
+
+#ifdef FBOB_TRACE
+FBOB_TRACE_IO(fbob_trace_io_bob)
+#endif

@@ -30,10 +30,9 @@ using tile::kT;
 // first backward on the tile skeleton
 // ===========================================================================
 struct DqParams {
-  CUtensorMap mQ, mdO;     // resident
   CUtensorMap mK, mV;      // streamed
+  const __nv_bfloat16 *Q, *dO;   // resident (copied into TMEM)
   const float *O, *L;
-  const __nv_bfloat16* dO;
   float *dQ, *D;
   int N;
   float tau;
@@ -42,42 +41,40 @@ struct DqParams {
   int stall;
 };
 
-// Row kernel: resident Q, dO; ring A = K (read by dQ += dS K), ring B = V
-// (read only by dP = dO V^T).  dS goes to TMEM (TS MMA).
+// Row kernel: resident Q, dO in TMEM (A operands of the score MMAs); ring A
+// = K (read by dQ += dS K), ring B = V (read only by dP = dO V^T).  dS goes to
+// TMEM (TS MMA).  TMEM: dQ (d) | [S | dP] x 2 | dS halves (2 x 16) | Q, dO (d).
 template <int D_>
 struct DqOp {
   using Params = DqParams;
   static constexpr int D = D_, DC = D / 64;
-  static constexpr int RES = 2 * DC * tile::kChunk;
+  static constexpr int RES = 0, TRES = 2;
   static constexpr int ACH = tile::kBlk, BCH = tile::kBlk;
   static constexpr int SA = DC * ACH, SB = DC * BCH, SA_TX = SA, SB_TX = SB;
-  static constexpr int NSA = 4, NSB = 4;
+  static constexpr int NSA = 8, NSB = 8;
   static constexpr bool VEC = false, ROW_SUMS = false, TS = true;
   static constexpr int VEC_OFF = 0, OPS = 0;
   static constexpr int ACC = D, SCOLS = 64, NBUF = 2;   // [S | dP]
   static constexpr int OP_HALF = 16, OP_COL = ACC + NBUF * SCOLS;
-  static constexpr int SMEM = RES + NSA * SA + NSB * SB;
-  static_assert(OP_COL + 2 * OP_HALF <= 512, "TMEM budget");
+  static constexpr int TRES_COL = OP_COL + 2 * OP_HALF;
+  static constexpr int SMEM = NSA * SA + NSB * SB;
+  static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
   static_assert(SMEM + 1024 <= 232448, "shared memory budget");
 
-  __device__ static void load_res(const Params& p, uint8_t* res, uint64_t* bar, int row0, int head) {
-    for (int kc = 0; kc < DC; ++kc) {
-      tma_load_3d(res + kc * tile::kChunk, &p.mQ, bar, kc * 64, row0, head);
-      tma_load_3d(res + (DC + kc) * tile::kChunk, &p.mdO, bar, kc * 64, row0, head);
-    }
-  }
+  __device__ static const void* tres_src(const Params& p, int s) { return s == 0 ? (const void*)p.Q : (const void*)p.dO; }
+  __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
   __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
     for (int kc = 0; kc < DC; ++kc) tma_load_3d(st + kc * ACH, &p.mK, bar, kc * 64, t * tile::kT, head);
   }
   __device__ static void load_b(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
     for (int kc = 0; kc < DC; ++kc) tma_load_3d(st + kc * BCH, &p.mV, bar, kc * 64, t * tile::kT, head);
   }
-  __device__ static void score_mmas(uint32_t sc, uint32_t res, uint32_t sa, uint32_t sb) {
+  __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t, uint32_t sa, uint32_t sb) {
     const uint32_t i32 = idesc_bf16(tile::kM, 32, false, false);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-      mma_ss_w(sc, tile::res_lo(res, 0, DC, k), tile::kmaj_lo(sa, ACH, 0, k), i32, k > 0);       // S
-      mma_ss_w(sc + 32, tile::res_lo(res, 1, DC, k), tile::kmaj_lo(sb, BCH, 0, k), i32, k > 0);  // dP
+      mma_ts_w(sc, tile::tres_a(tres, 0, D, k), tile::kmaj_lo(sa, ACH, 0, k), i32, k > 0);       // S = Q K^T
+      mma_ts_w(sc + 32, tile::tres_a(tres, 1, D, k), tile::kmaj_lo(sb, BCH, 0, k), i32, k > 0);  // dP = dO V^T
     }
   }
   __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
@@ -152,8 +149,8 @@ struct DqOp {
 };
 
 struct DkvParams {
-  CUtensorMap mK, mV;      // resident
   CUtensorMap mQ, mdO;     // streamed
+  const __nv_bfloat16 *K, *V;   // resident (copied into TMEM)
   const float *L, *D;
   float *dK, *dV;
   int N;
@@ -163,30 +160,28 @@ struct DkvParams {
   int stall;
 };
 
-// Column kernel: resident K, V; ring A = [Q | dO] + (L, D) of the tile.
-// P and dS go to TMEM (TS MMAs).
+// Column kernel: resident K, V in TMEM; ring A = [Q | dO] + (L, D) of the
+// tile.  P and dS go to TMEM (TS MMAs).  TMEM: dK, dV (2d) | [S^T | dP^T] x
+// NBUF | (P, dS) halves (2 x 32) | K, V (d); one score buffer at d = 128.
 template <int D_>
 struct DkvOp {
   using Params = DkvParams;
   static constexpr int D = D_, DC = D / 64;
-  static constexpr int RES = 2 * DC * tile::kChunk;
+  static constexpr int RES = 0, TRES = 2;
   static constexpr int ACH = 2 * tile::kBlk, VEC_OFF = DC * ACH;
   static constexpr int SA = DC * ACH + 1024, SA_TX = DC * ACH + 256, SB = 0, SB_TX = 0;
-  static constexpr int NSA = 4, NSB = 0;
+  static constexpr int NSA = 8, NSB = 0;
   static constexpr bool VEC = true, ROW_SUMS = false, TS = true;
   static constexpr int OPS = 0;
-  static constexpr int ACC = 2 * D, SCOLS = 64, NBUF = 2;   // dK, dV; [S^T | dP^T]
+  static constexpr int ACC = 2 * D, SCOLS = 64, NBUF = D == 128 ? 1 : 2;   // dK, dV; [S^T | dP^T]
   static constexpr int OP_HALF = 32, OP_COL = ACC + NBUF * SCOLS;
-  static constexpr int SMEM = RES + NSA * SA;
-  static_assert(OP_COL + 2 * OP_HALF <= 512, "TMEM budget");
+  static constexpr int TRES_COL = OP_COL + 2 * OP_HALF;
+  static constexpr int SMEM = NSA * SA;
+  static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
   static_assert(SMEM + 1024 <= 232448, "shared memory budget");
 
-  __device__ static void load_res(const Params& p, uint8_t* res, uint64_t* bar, int col0, int head) {
-    for (int kc = 0; kc < DC; ++kc) {
-      tma_load_3d(res + kc * tile::kChunk, &p.mK, bar, kc * 64, col0, head);
-      tma_load_3d(res + (DC + kc) * tile::kChunk, &p.mV, bar, kc * 64, col0, head);
-    }
-  }
+  __device__ static const void* tres_src(const Params& p, int s) { return s == 0 ? (const void*)p.K : (const void*)p.V; }
+  __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
   __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
     for (int kc = 0; kc < DC; ++kc) {
       tma_load_3d(st + kc * ACH, &p.mQ, bar, kc * 64, t * tile::kT, head);
@@ -197,12 +192,12 @@ struct DkvOp {
     tile::bulk_load(st + VEC_OFF + 128, p.D + v, 128, bar);
   }
   __device__ static void load_b(const Params&, uint8_t*, uint64_t*, int, int) {}
-  __device__ static void score_mmas(uint32_t sc, uint32_t res, uint32_t sa, uint32_t) {
+  __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t, uint32_t sa, uint32_t) {
     const uint32_t i32 = idesc_bf16(tile::kM, 32, false, false);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-      mma_ss_w(sc, tile::res_lo(res, 0, DC, k), tile::kmaj_lo(sa, ACH, 0, k), i32, k > 0);       // S^T
-      mma_ss_w(sc + 32, tile::res_lo(res, 1, DC, k), tile::kmaj_lo(sa, ACH, 1, k), i32, k > 0);  // dP^T
+      mma_ts_w(sc, tile::tres_a(tres, 0, D, k), tile::kmaj_lo(sa, ACH, 0, k), i32, k > 0);       // S^T = K Q^T
+      mma_ts_w(sc + 32, tile::tres_a(tres, 1, D, k), tile::kmaj_lo(sa, ACH, 1, k), i32, k > 0);  // dP^T = V dO^T
     }
   }
   __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
@@ -274,9 +269,9 @@ cudaError_t launch(const char* name, K kernel, int smem, int threads, dim3 grid,
 template <int D>
 cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
   DqParams q;
-  if (!make_bf16_map(&q.mQ, a.Q, a.BH, a.N, D, kM) || !make_bf16_map(&q.mdO, a.dO, a.BH, a.N, D, kM) ||
-      !make_bf16_map(&q.mK, a.K, a.BH, a.N, D, kT) || !make_bf16_map(&q.mV, a.V, a.BH, a.N, D, kT))
+  if (!make_bf16_map(&q.mK, a.K, a.BH, a.N, D, kT) || !make_bf16_map(&q.mV, a.V, a.BH, a.N, D, kT))
     return cudaErrorInvalidValue;
+  q.Q = static_cast<const __nv_bfloat16*>(a.Q);
   q.O = a.O;
   q.L = a.L;
   q.dO = static_cast<const __nv_bfloat16*>(a.dO);
@@ -291,9 +286,10 @@ cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
   cudaError_t e = launch("attn_bwd_dq", tile::tile_kernel<DqOp<D>>, DqOp<D>::SMEM, tile::kThreads, grid, q, s);
   if (e != cudaSuccess) return e;
   DkvParams k;
-  if (!make_bf16_map(&k.mK, a.K, a.BH, a.N, D, kM) || !make_bf16_map(&k.mV, a.V, a.BH, a.N, D, kM) ||
-      !make_bf16_map(&k.mQ, a.Q, a.BH, a.N, D, kT) || !make_bf16_map(&k.mdO, a.dO, a.BH, a.N, D, kT))
+  if (!make_bf16_map(&k.mQ, a.Q, a.BH, a.N, D, kT) || !make_bf16_map(&k.mdO, a.dO, a.BH, a.N, D, kT))
     return cudaErrorInvalidValue;
+  k.K = static_cast<const __nv_bfloat16*>(a.K);
+  k.V = static_cast<const __nv_bfloat16*>(a.V);
   k.L = a.L;
   k.D = a.D;
   k.dK = a.dK;
@@ -313,3 +309,7 @@ cudaError_t tc_bwd(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
 }
 
 }  // namespace fbob
+
+#ifdef FBOB_TRACE
+FBOB_TRACE_IO(fbob_trace_io_bwd)
+#endif

@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd2_tc(const __grid_constan
       bool ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.res_full, 0, wt));
       int ns = 0, na[2] = {0, nblk > 1 ? 0 : nt};
       uint64_t idle_since = 0;
+      uint32_t idle = 0;  // empty polls since the last check of the clock
       while (ok && (na[0] < nt || na[1] < nt)) {
         bool progressed = false;
         for (int x = 0; x < nblk; ++x) {
@@ -198,9 +199,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd2_tc(const __grid_constan
         }
         if (progressed) {
           idle_since = 0;
-        } else {
-          __nanosleep(20);
-          // lane 0 decides; the decision is broadcast so the warp stays converged
+        } else if ((++idle & 63u) == 0u) {
+          // Spin on the probes (a sleep here delays the next issue by far more
+          // than the tile period); every 64 empty polls lane 0 reads the clock
+          // and the abort flag, and the decision is broadcast so the warp stays
+          // converged.
           const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
           const int aborting = __shfl_sync(0xffffffffu, *wt.abort, 0);
           if (idle_since == 0) {

@@ -81,6 +81,22 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0u;
 }
 
+// Two non-blocking probes in one instruction group: the second does not wait
+// for the first one's result, so the pair costs about one probe's latency.
+__device__ __forceinline__ bool mbar_test2(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred q0, q1, q;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+      "and.pred q, q0, q1;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1)
+      : "memory");
+  return ok != 0u;
+}
+
 // Warp-uniform probe: lane 0's view, broadcast to the warp.
 __device__ __forceinline__ bool mbar_test_w(uint64_t* bar, uint32_t parity) {
   return __shfl_sync(0xffffffffu, (int)mbar_test(bar, parity), 0) != 0;

@@ -3,26 +3,36 @@
 // BoB pass 1 (query rows resident, key tiles streamed), BoB pass 2 (keys
 // resident, query tiles streamed) and the two first-backward kernels.
 //
-// CTA of 10 warps:
+// CTA of 11 warps:
 //   warps 0-7  two elementwise warpgroups; warpgroup g handles the streamed
 //              tiles t with t % 2 == g, so one group works on tile t while the
 //              other works on tile t+1.  Thread r of either group owns TMEM
 //              lane r = tile row r (row sums are thread-local).
 //   warp 8     TMA producer (one thread).
-//   warp 9     tcgen05.mma issuer (one thread) and TMEM owner (512 columns).
+//   warp 9     issues the score MMAs; TMEM owner (512 columns).
+//   warp 10    issues the accumulator MMAs.
+//
+// Resident operands of the score MMAs live in TMEM when the policy says so
+// (TRES > 0): at kernel start each elementwise warpgroup copies its share of
+// the resident rows from global memory into TMEM (lane r = resident row r,
+// two bf16 per column), and the score MMAs read them as the A operand (TS
+// MMA).  Only the streamed tile then comes from shared memory, which keeps
+// the 32- and 64-column score MMAs off the shared-memory bandwidth limit.
+// Residents the policy keeps in shared memory (RES > 0) arrive by TMA.
 //
 // Per 32-row streamed tile t:
 //   1. TMA fills ring A (operands the accumulator MMAs also read, plus any
-//      per-tile vectors) and ring B (operands only the score MMAs read).
+//      per-tile vectors) and ring B (operands only the score MMAs read); both
+//      stages of a tile complete one barrier.
 //   2. Score MMAs write fp32 score tiles into TMEM buffer t % NBUF; ring B's
 //      stage is released as soon as they complete.
 //   3. The owning warpgroup loads the scores, releases the TMEM buffer,
 //      computes bf16 operands and writes them to operand half t % 2 (shared
 //      memory for SS MMAs, TMEM for TS MMAs).
 //   4. Accumulator MMAs read the operand half and ring A's stage; their
-//      completion releases both.  The MMA thread issues whichever of the next
-//      score batch and the next accumulator batch is ready, so the tensor pipe
-//      works on later tiles while a warpgroup still computes operands.
+//      completion releases both.  Score and accumulator MMAs come from two
+//      warps, so the tensor pipe works on later tiles' scores while a
+//      warpgroup still computes tile t's operands.
 // Every wait is bounded (tc_ptx.cuh mbar_wait); on give-up every role leaves
 // its loop, copies and MMAs in flight are drained and TMEM is freed.
 //
@@ -41,16 +51,40 @@ namespace tile {
 
 using namespace tc;
 
+// Timeline instrumentation, compiled only with -DFBOB_TRACE: clock64 stamps of
+// CTA (0, 0) of the kernel whose layout id matches g_trace_sel, one slot per
+// (event, tile < 64).  Off in every normal build.
+#ifdef FBOB_TRACE
+static __device__ unsigned long long g_trace[16 * 64];
+static __device__ int g_trace_sel;
+#define FBOB_STAMP(ev, i)                                                                                  \
+  do {                                                                                                     \
+    if (trace_on && (i) < 64) g_trace[(ev)*64 + (i)] = clock64();                                          \
+  } while (0)
+#define FBOB_TRACE_IO(fn)                                                                                  \
+  extern "C" int fn(int sel, void* out) {                                                                  \
+    if (out) return (int)cudaMemcpyFromSymbol(out, fbob::tile::g_trace, sizeof(fbob::tile::g_trace));      \
+    static unsigned long long zero[16 * 64];                                                               \
+    cudaError_t e = cudaMemcpyToSymbol(fbob::tile::g_trace, zero, sizeof(zero));                           \
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(fbob::tile::g_trace_sel, &sel, sizeof(int));              \
+    return (int)e;                                                                                         \
+  }
+#else
+#define FBOB_STAMP(ev, i) \
+  do {                    \
+  } while (0)
+#endif
+
 constexpr int kM = 128;            // resident rows per CTA = TMEM lanes
 constexpr int kT = 32;             // streamed rows per tile
 constexpr int kEwWarps = 8;
-constexpr int kProdWarp = 8, kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kProdWarp = 8, kMmaWarp = 9, kAccWarp = 10;
+constexpr int kThreads = 352;
 constexpr int kChunk = 16384;      // 128 rows x 128 B: one 64-column chunk of a resident tile
 constexpr int kBlk = 4096;         // 32 rows x 128 B: one 64-column chunk of a streamed tensor
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kDrainNs = 200000000ull;
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 8;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -60,11 +94,12 @@ __device__ __forceinline__ float ex2(float x) {
 
 struct Ctrl {
   uint64_t res_full;
+  uint64_t tres_full;    // TMEM residents written (both warpgroups)
   uint64_t a_full[kMaxStages], a_empty[kMaxStages];
-  uint64_t b_full[kMaxStages], b_empty[kMaxStages];
+  uint64_t b_empty[kMaxStages];
   uint64_t s_full[2], s_empty[2];
   uint64_t o_full[2], o_empty[2];
-  uint64_t acc_full, drain;
+  uint64_t acc_full, drain, drain_acc;
   uint64_t red;          // epilogue: both warpgroups' row partials written
   uint32_t tmem_base;
   int abort_flag;
@@ -79,6 +114,10 @@ struct TileSync {
   int sa;         // ring-A stage of the tile
   bool vec;       // the tile's ring-A stage carries vectors read by the warpgroup
   bool ts;        // operands go to TMEM
+#ifdef FBOB_TRACE
+  bool trace_on;
+  int t;
+#endif
 
   // scores of this tile are in registers: the TMEM buffer may be reused
   __device__ __forceinline__ void release_scores() const {
@@ -87,7 +126,9 @@ struct TileSync {
   }
   // wait until the accumulator MMAs of this group's previous tile have read
   // the operand half
-  __device__ __forceinline__ bool acquire_ops() const { return mbar_wait(&c->o_empty[q], (k & 1) ^ 1, *w); }
+  __device__ __forceinline__ bool acquire_ops() const {
+    return mbar_wait(&c->o_empty[q], (k & 1) ^ 1, *w);
+  }
   // operands written: hand them to the MMA thread (and release the ring-A
   // vectors this warpgroup read)
   __device__ __forceinline__ void publish_ops() const {
@@ -139,6 +180,8 @@ struct TileArgs {
 
 template <class Op>
 __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant__ typename Op::Params p) {
+  static_assert(Op::NSB == 0 || Op::NSB == Op::NSA, "ring B stages pair with ring A stages");
+  static_assert(Op::NBUF < Op::NSA, "the MMA order needs more stages than score buffers");
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ Ctrl ctrl;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -152,14 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
   if (tid == 0) {
     ctrl.abort_flag = 0;
     mbar_init(&ctrl.res_full, 1);
+    mbar_init(&ctrl.tres_full, 256);
     for (int s = 0; s < Op::NSA; ++s) {
       mbar_init(&ctrl.a_full[s], 1);
       mbar_init(&ctrl.a_empty[s], Op::VEC ? 1 + 4 : 1);
     }
-    for (int s = 0; s < Op::NSB; ++s) {
-      mbar_init(&ctrl.b_full[s], 1);
-      mbar_init(&ctrl.b_empty[s], 1);
-    }
+    for (int s = 0; s < Op::NSB; ++s) mbar_init(&ctrl.b_empty[s], 1);
     for (int q = 0; q < 2; ++q) {
       mbar_init(&ctrl.s_full[q], 1);
       mbar_init(&ctrl.s_empty[q], 128);
@@ -168,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
     }
     mbar_init(&ctrl.acc_full, 1);
     mbar_init(&ctrl.drain, 1);
+    mbar_init(&ctrl.drain_acc, 1);
     mbar_init(&ctrl.red, 256);
     fence_mbar_init();
     if ((smem_u32(smem) & 1023u) != 0u) {  // layout assumption; never expected
@@ -185,108 +227,102 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
   const uint32_t tb = ctrl.tmem_base;
   const Waiter wt{&ctrl.abort_flag, p.err, p.wait_ns};
   const bool live = ctrl.abort_flag == 0;
+#ifdef FBOB_TRACE
+  constexpr int kTraceId = Op::ACC * 1000000 + Op::SCOLS * 1000 + Op::TRES * 100 + Op::OP_HALF;
+  const bool trace_cta = blockIdx.x == 0 && blockIdx.y == 0 && g_trace_sel == kTraceId && (tid & 31) == 0;
+  const bool trace_on = trace_cta && (warp >= kEwWarps || (warp & 3) == 0);
+#endif
 
   if (warp == kProdWarp) {
     // ------------------------------------------------------------------ TMA
+    // Ring A and ring B stages of tile t fill together and complete one
+    // barrier (a_full), so the MMA warp waits once per tile for its operands.
     if (live && (tid & 31) == 0) {
-      int ia = 0, ib = 0;
-      mbar_arrive_expect_tx(&ctrl.res_full, Op::RES);
-      Op::load_res(p, res, &ctrl.res_full, blk0, head);
+      int ia = 0;
+      if constexpr (Op::RES > 0) {
+        mbar_arrive_expect_tx(&ctrl.res_full, Op::RES);
+        Op::load_res(p, res, &ctrl.res_full, blk0, head);
+      }
       bool ok = true;
       for (int t = 0; t < nt && ok; ++t) {
         const int sa = t % Op::NSA;
         if (!(ok = mbar_wait(&ctrl.a_empty[sa], ((t / Op::NSA) & 1) ^ 1, wt))) break;
-        if (p.stall && t == 0) continue;  // test hook: nothing will fill this stage
-        mbar_arrive_expect_tx(&ctrl.a_full[sa], Op::SA_TX);
-        Op::load_a(p, ring_a + sa * Op::SA, &ctrl.a_full[sa], t, head);
-        ia = t + 1;
         if constexpr (Op::NSB > 0) {
-          const int sb = t % Op::NSB;
-          if (!(ok = mbar_wait(&ctrl.b_empty[sb], ((t / Op::NSB) & 1) ^ 1, wt))) break;
-          mbar_arrive_expect_tx(&ctrl.b_full[sb], Op::SB_TX);
-          Op::load_b(p, ring_b + sb * Op::SB, &ctrl.b_full[sb], t, head);
-          ib = t + 1;
+          if (!(ok = mbar_wait(&ctrl.b_empty[sa], ((t / Op::NSA) & 1) ^ 1, wt))) break;
         }
+        if (p.stall && t == 0) continue;  // test hook: nothing will fill this stage
+        mbar_arrive_expect_tx(&ctrl.a_full[sa], Op::SA_TX + (Op::NSB > 0 ? Op::SB_TX : 0));
+        Op::load_a(p, ring_a + sa * Op::SA, &ctrl.a_full[sa], t, head);
+        if constexpr (Op::NSB > 0) Op::load_b(p, ring_b + sa * Op::SB, &ctrl.a_full[sa], t, head);
+        FBOB_STAMP(7, t);
+        ia = t + 1;
       }
       if (!ok) {
         // give-up path: every copy already issued lands before the CTA exits
-        mbar_wait_drain(&ctrl.res_full, 0, kDrainNs);
+        if constexpr (Op::RES > 0) mbar_wait_drain(&ctrl.res_full, 0, kDrainNs);
         for (int t = (ia > Op::NSA ? ia - Op::NSA : 0); t < ia; ++t)
           mbar_wait_drain(&ctrl.a_full[t % Op::NSA], (t / Op::NSA) & 1, kDrainNs);
-        if constexpr (Op::NSB > 0) {
-          for (int t = (ib > Op::NSB ? ib - Op::NSB : 0); t < ib; ++t)
-            mbar_wait_drain(&ctrl.b_full[t % Op::NSB], (t / Op::NSB) & 1, kDrainNs);
-        }
       }
     }
   } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------------ MMA
-    // Score batches S(t) and accumulator batches A(u) are each issued in
-    // order; between them the thread issues whichever is ready (A first: it
-    // frees stages), so a warpgroup still computing A(u)'s operands does not
-    // hold back S(t+1).  Readiness is probed without blocking; one bounded
-    // timer covers any stretch without progress.
+    // --------------------------------------------------------- score MMAs
+    // Two warps issue MMAs: this one the score batches S(t), warp kAccWarp
+    // the accumulator batches A(t).  An mbarrier probe costs an issuing warp
+    // one to two hundred cycles, about as much as a batch of 32-column MMAs,
+    // so each warp pays only for its own waits and the tensor pipe takes
+    // work from both.  The two warps write disjoint TMEM (score buffers vs
+    // accumulators) and each commit tracks its own warp's MMAs.  Ring A's
+    // stage t is released by A(t)'s commit although S(t) also read it: A(t)
+    // needs tile t's operands, which exist only after S(t) completed.
+    // S(t) waits for its stage and, for t >= NBUF, for tile t - NBUF's
+    // warpgroup to have read the score buffer; no wait depends on work issued
+    // later (NBUF < NSA), so the order cannot deadlock.
     if (live) {  // the whole warp runs the loop; lane 0 issues (elect.sync)
       const uint32_t res_l = desc_lo(smem_u32(res), 16), ra = smem_u32(ring_a), rb = smem_u32(ring_b);
-      const uint32_t ops_a = Op::TS ? (tb + Op::OP_COL) : desc_lo(smem_u32(ops), 16);
-      bool ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.res_full, 0, wt));
-      int ns = 0, na = 0;  // next score batch, next accumulator batch
-      uint64_t idle_since = 0;
-      while (ok && na < nt) {
-        bool progressed = false;
-        if (na < ns && mbar_test_w(&ctrl.o_full[na & 1], (na >> 1) & 1)) {
-          tc_fence_after();
-          Op::accum_mmas(tb, ops_a, ra + (na % Op::NSA) * Op::SA, na & 1, na == 0);
-          mma_commit_w(&ctrl.o_empty[na & 1]);
-          mma_commit_w(&ctrl.a_empty[na % Op::NSA]);
-          ++na;
-          progressed = true;
-        }
-        if (ns < nt) {
-          const int t = ns;
-          bool ready = mbar_test_w(&ctrl.a_full[t % Op::NSA], (t / Op::NSA) & 1);
-          uint32_t stage_b = rb;
-          if constexpr (Op::NSB > 0) {
-            ready = ready && mbar_test_w(&ctrl.b_full[t % Op::NSB], (t / Op::NSB) & 1);
-            stage_b = rb + (t % Op::NSB) * Op::SB;
-          }
-          if (ready && t >= Op::NBUF) {  // the previous user of this score buffer has read it
-            const int u = t - Op::NBUF;
-            ready = mbar_test_w(&ctrl.s_empty[u & 1], (u >> 1) & 1);
-          }
-          if (ready) {
-            tc_fence_after();
-            Op::score_mmas(tb + Op::ACC + (t % Op::NBUF) * Op::SCOLS, res_l, desc_lo(ra + (t % Op::NSA) * Op::SA, 16),
-                           desc_lo(stage_b, 16));
-            mma_commit_w(&ctrl.s_full[t & 1]);
-            if constexpr (Op::NSB > 0) mma_commit_w(&ctrl.b_empty[t % Op::NSB]);
-            ++ns;
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          idle_since = 0;
-        } else {
-          __nanosleep(20);
-          // lane 0 decides; the decision is broadcast so the warp stays converged
-          const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
-          const int aborting = __shfl_sync(0xffffffffu, *wt.abort, 0);
-          if (idle_since == 0) {
-            idle_since = now;
-          } else if (aborting) {
-            ok = false;
-          } else if (now - idle_since > wt.limit) {
-            if ((tid & 31) == 0) {
-              *wt.abort = 1;
-              atomicOr(p.err, kErrTimeout);
-            }
-            ok = false;
-          }
-        }
+      bool ok = true;
+      if constexpr (Op::RES > 0) ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.res_full, 0, wt));
+      if constexpr (Op::TRES > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(&ctrl.tres_full, 0, wt));
+      const uint32_t tres = tb + Op::TRES_COL;
+      for (int t = 0; ok && t < nt; ++t) {
+        const int sa = t % Op::NSA, u = t - Op::NBUF;
+        // both conditions probed in one go (their latencies overlap); the
+        // bounded blocking waits only run when a probe found one incomplete
+        uint64_t* eb = &ctrl.s_empty[(u < 0 ? 0 : u) & 1];
+        const uint32_t ep = u < 0 ? 1u : (uint32_t)((u >> 1) & 1);   // parity 1 of a fresh barrier: complete
+        if (!__all_sync(0xffffffffu, mbar_test2(&ctrl.a_full[sa], (t / Op::NSA) & 1, eb, ep)))
+          ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.a_full[sa], (t / Op::NSA) & 1, wt) &&
+                                           (u < 0 || mbar_wait(&ctrl.s_empty[u & 1], (u >> 1) & 1, wt)));
+        if (!ok) break;
+        tc_fence_after();
+        FBOB_STAMP(9, t);
+        Op::score_mmas(tb + Op::ACC + (t % Op::NBUF) * Op::SCOLS, tres, res_l, desc_lo(ra + sa * Op::SA, 16),
+                       desc_lo(rb + sa * Op::SB, 16));
+        mma_commit_w(&ctrl.s_full[t & 1]);
+        if constexpr (Op::NSB > 0) mma_commit_w(&ctrl.b_empty[sa]);
+        FBOB_STAMP(0, t);
       }
-      if (ok) mma_commit_w(&ctrl.acc_full);
       mma_commit_w(&ctrl.drain);
       mbar_wait_drain(&ctrl.drain, 0, kDrainNs);
+    }
+  } else if (warp == kAccWarp) {
+    // --------------------------------------------------- accumulator MMAs
+    if (live) {
+      const uint32_t ra = smem_u32(ring_a);
+      const uint32_t ops_a = Op::TS ? (tb + Op::OP_COL) : desc_lo(smem_u32(ops), 16);
+      bool ok = true;
+      for (int t = 0; ok && t < nt; ++t) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.o_full[t & 1], (t >> 1) & 1, wt));
+        if (!ok) break;
+        tc_fence_after();
+        FBOB_STAMP(10, t);
+        Op::accum_mmas(tb, ops_a, ra + (t % Op::NSA) * Op::SA, t & 1, t == 0);
+        mma_commit_w(&ctrl.o_empty[t & 1]);
+        mma_commit_w(&ctrl.a_empty[t % Op::NSA]);
+        FBOB_STAMP(1, t);
+      }
+      if (ok) mma_commit_w(&ctrl.acc_full);
+      mma_commit_w(&ctrl.drain_acc);
+      mbar_wait_drain(&ctrl.drain_acc, 0, kDrainNs);
     }
   } else {
     // ------------------------------------------------------------ elementwise
@@ -294,14 +330,44 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
     const int r = tid & 127;                 // tile row = TMEM lane
     const uint32_t lane = (uint32_t)((warp & 3) * 32) << 16;
     typename Op::Row row;
+    if constexpr (Op::TRES > 0) {
+      // resident rows -> TMEM: warpgroup g copies residents g, g + 2, ...
+      const size_t row_g = (size_t)head * p.N + blk0 + r;
+      for (int s = g; s < Op::TRES; s += 2) {
+        const uint4* src = reinterpret_cast<const uint4*>(Op::tres_src(p, s)) + row_g * (Op::D / 8);
+        const uint32_t col = tb + lane + Op::TRES_COL + (uint32_t)(s * (Op::D / 2));
+#pragma unroll
+        for (int c = 0; c < Op::D / 32; ++c) {  // 16 columns = 32 bf16 per store
+          uint32_t w[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 u = src[4 * c + q];
+            w[4 * q] = u.x;
+            w[4 * q + 1] = u.y;
+            w[4 * q + 2] = u.z;
+            w[4 * q + 3] = u.w;
+          }
+          tmem_st16_nowait(col + 16 * c, w);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&ctrl.tres_full);
+    }
     Op::ew_init(row, p, blk0, r, head);
     bool ok = live;
     for (int t = g; t < nt && ok; t += 2) {
       const int k = t >> 1, sa = t % Op::NSA;
+      FBOB_STAMP(8, t);
       if (Op::VEC && !mbar_wait(&ctrl.a_full[sa], (t / Op::NSA) & 1, wt)) { ok = false; break; }
       if (!mbar_wait(&ctrl.s_full[g], k & 1, wt)) { ok = false; break; }
+      FBOB_STAMP(2, t);
       tc_fence_after();
+#ifdef FBOB_TRACE
+      const TileSync sync{&ctrl, &wt, g, k, sa, Op::VEC, Op::TS, trace_on, t};
+#else
       const TileSync sync{&ctrl, &wt, g, k, sa, Op::VEC, Op::TS};
+#endif
       TileArgs ta;
       ta.sc = tb + lane + Op::ACC + (t % Op::NBUF) * Op::SCOLS;
       ta.vec = Op::VEC ? reinterpret_cast<const float*>(ring_a + sa * Op::SA + Op::VEC_OFF) : nullptr;
@@ -309,6 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
       ta.h = (uint32_t)g;
       ta.t = t;
       ok = Op::ew_tile(row, p, ta, sync, r);
+      FBOB_STAMP(6, t);
+#ifdef FBOB_TRACE
+      if (trace_cta && t < 64) g_trace[(11 + (warp & 3)) * 64 + t] = clock64();
+#endif
     }
     const EpiArgs ea{tb + lane, reinterpret_cast<float*>(ring_a), &ctrl, &wt, blk0, r, head, g};
     if (ok && mbar_wait(&ctrl.acc_full, 0, wt)) {
@@ -333,6 +403,11 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
 // Descriptor low words (see tc_ptx.cuh desc_lo).  Offsets are in bytes and
 // compile-time constants once the k loops are unrolled, so each operand of an
 // MMA costs one add.
+// TMEM-resident operand `slot` (d/2 columns each, two bf16 per column), k-th
+// 16-element step: the A address of a TS MMA.
+__device__ __forceinline__ uint32_t tres_a(uint32_t tres, int slot, int d, int k) {
+  return tres + (uint32_t)(slot * (d / 2) + k * 8);
+}
 // K-major resident tile: slot of `dc` 64-column chunks of 16 KB, k-th 16-column step.
 __device__ __forceinline__ uint32_t res_lo(uint32_t res_lo0, int slot, int dc, int k) {
   return res_lo0 + (uint32_t)(((slot * dc + (k >> 2)) * kChunk + (k & 3) * 32) >> 4);
