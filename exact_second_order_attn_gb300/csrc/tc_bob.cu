@@ -52,10 +52,9 @@ namespace {
 using namespace tc;
 using namespace tile;
 
-enum Role { kU1 = 0, kZ = 1, kY = 2 };
-
 struct P1Params {
-  CUtensorMap mK, mUK, mV, mUV;              // streamed, box {64, 32}
+  CUtensorMap mK, mUK, mV, mUV;              // streamed, box {64, 32} (U1 sweep)
+  CUtensorMap mK64, mUK64, mV64, mUV64;      // streamed, box {64, 64} (Z and Y sweeps)
   const __nv_bfloat16 *Q, *UQ, *dO;          // resident (copied into TMEM)
   const float *L, *D, *O;
   float *gQ, *gdO, *ws;
@@ -82,102 +81,67 @@ struct P2Params {
 // ===========================================================================
 // pass 1
 // ===========================================================================
-template <int D_, int ROLE>
-struct Pass1 {
+__device__ __forceinline__ void load_tile2(const CUtensorMap* m0, const CUtensorMap* m1, uint8_t* st, int dc, int ch,
+                                           int blk, uint64_t* bar, int row, int head) {
+  for (int kc = 0; kc < dc; ++kc) {
+    tma_load_3d(st + kc * ch, m0, bar, kc * 64, row, head);
+    if (m1) tma_load_3d(st + kc * ch + blk, m1, bar, kc * 64, row, head);
+  }
+}
+
+// U1 sweep (32 keys per tile): U1 += dS UK + X K, alpha, EX.  Ring A = [K UK]
+// (also read by the accumulator MMAs), ring B = [V UV].
+template <int D_>
+struct PassU1 {
   using Params = P1Params;
-  static constexpr int D = D_, DC = D / 64;
-  static constexpr int RES = 0;
-  static constexpr int TRES = ROLE == kU1 ? 3 : 2;   // U1: Q UQ dO;  Z: Q dO;  Y: Q UQ
-  // ring A holds what the accumulator MMAs read, ring B what only the score
-  // MMAs read:  U1: A = [K UK], B = [V UV];  Z: A = K, B = V;  Y: A = [V UV], B = [K UK]
-  static constexpr int ABLK = ROLE == kZ ? 1 : 2, BBLK = ABLK;
-  static constexpr int ACH = ABLK * kBlk, BCH = BBLK * kBlk;
+  static constexpr int D = D_, DC = D / 64, T = 32;
+  static constexpr int RES = 0, TRES = 3;   // Q, UQ, dO
+  static constexpr int ACH = 2 * kBlk, BCH = 2 * kBlk;
   static constexpr int SA = DC * ACH, SB = DC * BCH, SA_TX = SA, SB_TX = SB;
-  static constexpr int NSA = (D == 128 && ROLE != kZ) ? 6 : 8, NSB = NSA;
-  static constexpr bool VEC = false;
-  static constexpr int VEC_OFF = 0;
-  static constexpr bool ROW_SUMS = ROLE != kZ;
-  static constexpr bool TS = true;
-  static constexpr int OPS = 0;
-  static constexpr int ACC = D;
-  static constexpr int SCOLS = ROLE == kU1 ? 128 : 64;   // [S|B|dP|C], [S|dP] or [S|B]
-  static constexpr int NBUF = (ROLE == kU1 && D == 128) ? 1 : 2;
-  static constexpr int OP_HALF = ROLE == kZ ? 16 : 32;   // (dS, X), G or (P, PB)
+  static constexpr int NSA = D == 128 ? 6 : 8, NSB = NSA;
+  static constexpr bool VEC = false, ROW_SUMS = true, TS = true;
+  static constexpr int VEC_OFF = 0, OPS = 0;
+  static constexpr int ACC = D, SCOLS = 128;           // [S|B|dP|C]
+  static constexpr int NBUF = D == 128 ? 1 : 2;
+  static constexpr int OP_HALF = 32;                    // dS, X
   static constexpr int OP_COL = ACC + NBUF * SCOLS;
   static constexpr int TRES_COL = OP_COL + 2 * OP_HALF;
   static constexpr int SMEM = NSA * SA + NSB * SB;
   static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
   static_assert(SMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
-  static_assert(NSA <= kMaxStages && NSB <= kMaxStages, "stage count");
 
   __device__ static const void* tres_src(const Params& p, int s) {
-    if (ROLE == kU1) return s == 0 ? (const void*)p.Q : s == 1 ? (const void*)p.UQ : (const void*)p.dO;
-    if (ROLE == kZ) return s == 0 ? (const void*)p.Q : (const void*)p.dO;
-    return s == 0 ? (const void*)p.Q : (const void*)p.UQ;
+    return s == 0 ? (const void*)p.Q : s == 1 ? (const void*)p.UQ : (const void*)p.dO;
   }
   __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
-  __device__ static void load_pair(const CUtensorMap* m0, const CUtensorMap* m1, uint8_t* st, int ch, uint64_t* bar,
-                                   int t, int head) {
-    for (int kc = 0; kc < DC; ++kc) {
-      tma_load_3d(st + kc * ch, m0, bar, kc * 64, t * kT, head);
-      if (m1) tma_load_3d(st + kc * ch + kBlk, m1, bar, kc * 64, t * kT, head);
-    }
-  }
   __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
-    if (ROLE == kU1) load_pair(&p.mK, &p.mUK, st, ACH, bar, t, head);
-    if (ROLE == kZ) load_pair(&p.mK, nullptr, st, ACH, bar, t, head);
-    if (ROLE == kY) load_pair(&p.mV, &p.mUV, st, ACH, bar, t, head);
+    load_tile2(&p.mK, &p.mUK, st, DC, ACH, kBlk, bar, t * T, head);
   }
   __device__ static void load_b(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
-    if (ROLE == kU1) load_pair(&p.mV, &p.mUV, st, BCH, bar, t, head);
-    if (ROLE == kZ) load_pair(&p.mV, nullptr, st, BCH, bar, t, head);
-    if (ROLE == kY) load_pair(&p.mK, &p.mUK, st, BCH, bar, t, head);
+    load_tile2(&p.mV, &p.mUV, st, DC, BCH, kBlk, bar, t * T, head);
   }
-
   __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t, uint32_t sa, uint32_t sb) {
     const uint32_t i64 = idesc_bf16(kM, 64, false, false), i32 = idesc_bf16(kM, 32, false, false);
-    if (ROLE == kZ) {
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        mma_ts_w(sc, tres_a(tres, 0, D, k), kmaj_lo(sa, ACH, 0, k), i32, k > 0);       // S = Q K^T
-        mma_ts_w(sc + 32, tres_a(tres, 1, D, k), kmaj_lo(sb, BCH, 0, k), i32, k > 0);  // dP = dO V^T
-      }
-      return;
-    }
-    const uint32_t kst = ROLE == kU1 ? sa : sb;   // the [K | UK] tile
-    const int kch = ROLE == kU1 ? ACH : BCH;
 #pragma unroll
     for (int k = 0; k < D / 16; ++k)  // [S | Q UK^T] = Q [K; UK]^T
-      mma_ts_w(sc, tres_a(tres, 0, D, k), kmaj_lo(kst, kch, 0, k), i64, k > 0);
+      mma_ts_w(sc, tres_a(tres, 0, D, k), kmaj(sa, ACH, 0, k), i64, k > 0);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k)  // B += UQ K^T
-      mma_ts_w(sc + 32, tres_a(tres, 1, D, k), kmaj_lo(kst, kch, 0, k), i32, 1);
-    if (ROLE == kU1) {
+      mma_ts_w(sc + 32, tres_a(tres, 1, D, k), kmaj(sa, ACH, 0, k), i32, 1);
 #pragma unroll
-      for (int k = 0; k < D / 16; ++k)  // [dP | C] = dO [V; UV]^T
-        mma_ts_w(sc + 64, tres_a(tres, 2, D, k), kmaj_lo(sb, BCH, 0, k), i64, k > 0);
-    }
+    for (int k = 0; k < D / 16; ++k)  // [dP | C] = dO [V; UV]^T
+      mma_ts_w(sc + 64, tres_a(tres, 2, D, k), kmaj(sb, BCH, 0, k), i64, k > 0);
   }
-
   __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
     const uint32_t amn = desc_lo(sa, ACH);
     const uint32_t id = idesc_bf16(kM, D, false, true);
 #pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
+    for (int kk = 0; kk < T / 16; ++kk) {
       const uint32_t a = ops + h * OP_HALF + kk * 8;
-      if (ROLE == kU1) {
-        mma_ts_w(tb, a, mn_lo(amn, 1, kk), id, acc0);   // U1 += dS UK
-        mma_ts_w(tb, a + 16, mn_lo(amn, 0, kk), id, 1);  // U1 += X K
-      } else if (ROLE == kZ) {
-        mma_ts_w(tb, a, mn_lo(amn, 0, kk), id, acc0);   // Z += G K
-      } else {
-        mma_ts_w(tb, a, mn_lo(amn, 1, kk), id, acc0);   // Y += P UV
-        mma_ts_w(tb, a + 16, mn_lo(amn, 0, kk), id, 1);  // Y += PB V
-      }
+      mma_ts_w(tb, a, mnmaj(amn, kBlk, kk), id, (first && kk == 0) ? 0u : 1u);  // U1 += dS UK
+      mma_ts_w(tb, a + 16, mnmaj(amn, 0, kk), id, 1);                            // U1 += X K
     }
   }
-
   struct Row {
     float nL, Di, alpha, ex;
   };
@@ -187,88 +151,268 @@ struct Pass1 {
     w.Di = p.D[vo];
     w.alpha = 0.f;
     w.ex = 0.f;
-    if (ROLE == kZ) {  // row totals of the U1 kernel; EX = E - D alpha
-      w.alpha = p.ws[2 * vo];
-      w.ex = fmaf(-w.Di, w.alpha, p.ws[2 * vo + 1]);
-    }
   }
-
   __device__ static bool ew_tile(Row& w, const Params& p, const TileArgs& a, const TileSync& s, int) {
     const float sc = p.tau * kLog2e;
-    uint32_t w0[16], w1[16];
+    uint32_t wdS[16], wX[16];
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      float S[16], X1[16], dP[16], C[16];   // X1 = B (U1, Y) or dP (Z)
-      if (ROLE == kU1)
-        tmem_ld16x4(a.sc + q * 16, a.sc + 32 + q * 16, a.sc + 64 + q * 16, a.sc + 96 + q * 16, S, X1, dP, C);
-      else
-        tmem_ld16x2(a.sc + q * 16, a.sc + 32 + q * 16, S, X1);
+      float S[16], B[16], dP[16], C[16];
+      tmem_ld16x4(a.sc + q * 16, a.sc + 32 + q * 16, a.sc + 64 + q * 16, a.sc + 96 + q * 16, S, B, dP, C);
       if (q == 1) s.release_scores();
 #pragma unroll
       for (int j = 0; j < 16; j += 2) {
-        float v0[2], v1[2] = {0.f, 0.f};
+        float ds[2], x[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const float pe = ex2(fmaf(S[j + e], sc, w.nL));
-          if (ROLE == kZ) {
-            const float ds = pe * (X1[j + e] - w.Di);
-            v0[e] = fmaf(w.ex, pe, w.alpha * ds);   // G = EX P + alpha dS
-          } else {
-            const float be = p.tau * X1[j + e];
-            const float pb = pe * be;
-            w.alpha += pb;
-            if (ROLE == kU1) {
-              const float te = dP[j + e] - w.Di;
-              v0[e] = pe * te;                        // dS
-              v1[e] = pe * fmaf(be, te, C[j + e]);    // X
-              w.ex += v1[e];
-            } else {
-              v0[e] = pe;                             // P
-              v1[e] = pb;                             // PB
-            }
-          }
+          const float be = p.tau * B[j + e];
+          const float te = dP[j + e] - w.Di;
+          w.alpha = fmaf(pe, be, w.alpha);
+          ds[e] = pe * te;
+          x[e] = pe * fmaf(be, te, C[j + e]);
+          w.ex += x[e];
         }
-        const int k = q * 8 + j / 2;
-        w0[k] = pack_bf16x2(v0[0], v0[1]);
-        w1[k] = pack_bf16x2(v1[0], v1[1]);
+        wdS[q * 8 + j / 2] = pack_bf16x2(ds[0], ds[1]);
+        wX[q * 8 + j / 2] = pack_bf16x2(x[0], x[1]);
       }
     }
     if (!s.acquire_ops()) return false;
-    tmem_st16_nowait(a.ops, w0);
-    if (ROLE != kZ) tmem_st16_nowait(a.ops + 16, w1);
+    tmem_st16_nowait(a.ops, wdS);
+    tmem_st16_nowait(a.ops + 16, wX);
     s.publish_ops();
     return true;
   }
-
   __device__ static void epilogue(Row& w, const Params& p, const EpiArgs& e) {
     float alpha = w.alpha, ex = w.ex;
-    if (ROW_SUMS && !e.sum_rows(alpha, ex)) return;
+    if (!e.sum_rows(alpha, ex)) return;
     const size_t vo = (size_t)e.head * p.N + e.blk0 + e.r;
     const size_t ro = vo * D;
     const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
 #pragma unroll 1
     for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
-      float acc[16], o[16];
+      float acc[16];
       tmem_ld16(e.tm + c0, acc);
-      if (ROLE == kU1) {
-        store16(p.gQ + ro + c0, acc);   // U1, finished by the Z kernel
-      } else {
-        const float4* src = reinterpret_cast<const float4*>((ROLE == kZ ? p.gQ : p.O) + ro + c0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 v = src[q];
-          const float u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            o[4 * q + i] = ROLE == kZ ? p.tau * (u[i] - acc[4 * q + i])     // gQ = tau (U1 - Z)
-                                      : fmaf(-alpha, u[i], acc[4 * q + i]);  // gdO = Y - alpha O
-        }
-        store16((ROLE == kZ ? p.gQ : p.gdO) + ro + c0, o);
-      }
+      store16(p.gQ + ro + c0, acc);   // U1, finished by the Z sweep
     }
-    if (ROLE == kU1 && e.g == 0) {
+    if (e.g == 0) {
       p.ws[2 * vo] = alpha;
       p.ws[2 * vo + 1] = fmaf(w.Di, alpha, ex);
+    }
+  }
+};
+
+// Z sweep (64 keys per tile): Z += G K, G = EX P + alpha dS, gQ = tau (U1 - Z).
+// Ring A = K, ring B = V.  G goes to TMEM at d = 64, to shared memory at d = 128.
+template <int D_>
+struct PassZ {
+  using Params = P1Params;
+  static constexpr int D = D_, DC = D / 64, T = 64, BLK = T * 128;
+  static constexpr int RES = 0, TRES = 2;   // Q, dO
+  static constexpr int ACH = BLK, BCH = BLK;
+  static constexpr int SA = DC * ACH, SB = DC * BCH, SA_TX = SA, SB_TX = SB;
+  static constexpr int NSA = D == 128 ? 5 : 8, NSB = NSA;
+  static constexpr bool VEC = false, ROW_SUMS = false, TS = D == 64;
+  static constexpr int VEC_OFF = 0;
+  static constexpr int OPS = TS ? 0 : 2 * kChunk;
+  static constexpr int ACC = D, SCOLS = 2 * T, NBUF = 2;   // [S | dP]
+  static constexpr int OP_HALF = T / 2, OP_COL = ACC + NBUF * SCOLS;
+  static constexpr int TRES_COL = OP_COL + (TS ? 2 * OP_HALF : 0);
+  static constexpr int SMEM = NSA * SA + NSB * SB + OPS;
+  static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
+  static_assert(SMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
+
+  __device__ static const void* tres_src(const Params& p, int s) { return s == 0 ? (const void*)p.Q : (const void*)p.dO; }
+  __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
+  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
+    load_tile2(&p.mK64, nullptr, st, DC, ACH, BLK, bar, t * T, head);
+  }
+  __device__ static void load_b(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
+    load_tile2(&p.mV64, nullptr, st, DC, BCH, BLK, bar, t * T, head);
+  }
+  __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t, uint32_t sa, uint32_t sb) {
+    const uint32_t i64 = idesc_bf16(kM, T, false, false);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      mma_ts_w(sc, tres_a(tres, 0, D, k), kmaj(sa, ACH, 0, k), i64, k > 0);      // S = Q K^T
+      mma_ts_w(sc + T, tres_a(tres, 1, D, k), kmaj(sb, BCH, 0, k), i64, k > 0);  // dP = dO V^T
+    }
+  }
+  __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
+    const uint32_t amn = desc_lo(sa, ACH);
+    const uint32_t id = idesc_bf16(kM, D, false, true);
+#pragma unroll
+    for (int kk = 0; kk < T / 16; ++kk) {  // Z += G K
+      const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+      if (TS)
+        mma_ts_w(tb, ops + h * OP_HALF + kk * 8, mnmaj(amn, 0, kk), id, acc);
+      else
+        mma_ss_w(tb, op64_lo(ops, 0, h, kk), mnmaj(amn, 0, kk), id, acc);
+    }
+  }
+  struct Row {
+    float nL, Di, alpha, ex;
+  };
+  __device__ static void ew_init(Row& w, const Params& p, int blk0, int r, int head) {
+    const size_t vo = (size_t)head * p.N + blk0 + r;
+    w.nL = -p.L[vo] * kLog2e;
+    w.Di = p.D[vo];
+    w.alpha = p.ws[2 * vo];                              // row totals of the U1 sweep
+    w.ex = fmaf(-w.Di, w.alpha, p.ws[2 * vo + 1]);       // EX = E - D alpha
+  }
+  __device__ static bool ew_tile(Row& w, const Params& p, const TileArgs& a, const TileSync& s, int r) {
+    const float sc = p.tau * kLog2e;
+    uint32_t wg[T / 2];
+#pragma unroll
+    for (int q = 0; q < T / 16; ++q) {
+      float S[16], dP[16];
+      tmem_ld16x2(a.sc + q * 16, a.sc + T + q * 16, S, dP);
+      if (q == T / 16 - 1) s.release_scores();
+#pragma unroll
+      for (int j = 0; j < 16; j += 2) {
+        float g[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float pe = ex2(fmaf(S[j + e], sc, w.nL));
+          g[e] = pe * fmaf(w.alpha, dP[j + e] - w.Di, w.ex);   // EX P + alpha dS
+        }
+        wg[q * 8 + j / 2] = pack_bf16x2(g[0], g[1]);
+      }
+    }
+    if (!s.acquire_ops()) return false;
+    if (TS) {
+      tmem_st16_nowait(a.ops, wg);
+      tmem_st16_nowait(a.ops + 16, wg + 16);
+    } else {
+      write_op64(a.ops + a.h * kChunk, (uint32_t)r, wg);
+    }
+    s.publish_ops();
+    return true;
+  }
+  __device__ static void epilogue(Row&, const Params& p, const EpiArgs& e) {
+    const size_t ro = ((size_t)e.head * p.N + e.blk0 + e.r) * D;
+    const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
+#pragma unroll 1
+    for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+      float z[16], o[16];
+      tmem_ld16(e.tm + c0, z);
+      const float4* u1 = reinterpret_cast<const float4*>(p.gQ + ro + c0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = u1[q];
+        o[4 * q] = p.tau * (v.x - z[4 * q]);
+        o[4 * q + 1] = p.tau * (v.y - z[4 * q + 1]);
+        o[4 * q + 2] = p.tau * (v.z - z[4 * q + 2]);
+        o[4 * q + 3] = p.tau * (v.w - z[4 * q + 3]);
+      }
+      store16(p.gQ + ro + c0, o);
+    }
+  }
+};
+
+// Y sweep (64 keys per tile): Y += P UV + PB V, alpha; gdO = Y - alpha O.
+// Ring A = [V UV] (read by the accumulator MMAs), ring B = [K UK].  P and PB
+// go to TMEM; one score buffer at d = 128.
+template <int D_>
+struct PassY {
+  using Params = P1Params;
+  static constexpr int D = D_, DC = D / 64, T = 64, BLK = T * 128;
+  static constexpr int RES = 0, TRES = 2;   // Q, UQ
+  static constexpr int ACH = 2 * BLK, BCH = 2 * BLK;
+  static constexpr int SA = DC * ACH, SB = DC * BCH, SA_TX = SA, SB_TX = SB;
+  static constexpr int NSA = D == 128 ? 3 : 6, NSB = NSA;
+  static constexpr bool VEC = false, ROW_SUMS = true, TS = true;
+  static constexpr int VEC_OFF = 0, OPS = 0;
+  static constexpr int ACC = D, SCOLS = 2 * T, NBUF = D == 128 ? 1 : 2;   // [S | B]
+  static constexpr int OP_HALF = T;                     // P, PB (32 columns each)
+  static constexpr int OP_COL = ACC + NBUF * SCOLS;
+  static constexpr int TRES_COL = OP_COL + 2 * OP_HALF;
+  static constexpr int SMEM = NSA * SA + NSB * SB;
+  static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
+  static_assert(SMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
+
+  __device__ static const void* tres_src(const Params& p, int s) { return s == 0 ? (const void*)p.Q : (const void*)p.UQ; }
+  __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
+  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
+    load_tile2(&p.mV64, &p.mUV64, st, DC, ACH, BLK, bar, t * T, head);
+  }
+  __device__ static void load_b(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
+    load_tile2(&p.mK64, &p.mUK64, st, DC, BCH, BLK, bar, t * T, head);
+  }
+  __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t, uint32_t, uint32_t sb) {
+    const uint32_t i128 = idesc_bf16(kM, 2 * T, false, false), i64 = idesc_bf16(kM, T, false, false);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k)  // [S | Q UK^T] = Q [K; UK]^T
+      mma_ts_w(sc, tres_a(tres, 0, D, k), kmaj(sb, BCH, 0, k), i128, k > 0);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k)  // B += UQ K^T
+      mma_ts_w(sc + T, tres_a(tres, 1, D, k), kmaj(sb, BCH, 0, k), i64, 1);
+  }
+  __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
+    const uint32_t amn = desc_lo(sa, ACH);
+    const uint32_t id = idesc_bf16(kM, D, false, true);
+#pragma unroll
+    for (int kk = 0; kk < T / 16; ++kk) {
+      const uint32_t a = ops + h * OP_HALF + kk * 8;
+      mma_ts_w(tb, a, mnmaj(amn, BLK, kk), id, (first && kk == 0) ? 0u : 1u);  // Y += P UV
+      mma_ts_w(tb, a + T / 2, mnmaj(amn, 0, kk), id, 1);                        // Y += PB V
+    }
+  }
+  struct Row {
+    float nL, alpha;
+  };
+  __device__ static void ew_init(Row& w, const Params& p, int blk0, int r, int head) {
+    w.nL = -p.L[(size_t)head * p.N + blk0 + r] * kLog2e;
+    w.alpha = 0.f;
+  }
+  __device__ static bool ew_tile(Row& w, const Params& p, const TileArgs& a, const TileSync& s, int) {
+    const float sc = p.tau * kLog2e;
+    uint32_t wP[T / 2], wPB[T / 2];
+#pragma unroll
+    for (int q = 0; q < T / 16; ++q) {
+      float S[16], B[16];
+      tmem_ld16x2(a.sc + q * 16, a.sc + T + q * 16, S, B);
+      if (q == T / 16 - 1) s.release_scores();
+#pragma unroll
+      for (int j = 0; j < 16; j += 2) {
+        float pv[2], pb[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          pv[e] = ex2(fmaf(S[j + e], sc, w.nL));
+          pb[e] = pv[e] * (p.tau * B[j + e]);
+          w.alpha += pb[e];
+        }
+        wP[q * 8 + j / 2] = pack_bf16x2(pv[0], pv[1]);
+        wPB[q * 8 + j / 2] = pack_bf16x2(pb[0], pb[1]);
+      }
+    }
+    if (!s.acquire_ops()) return false;
+    tmem_st16_nowait(a.ops, wP);
+    tmem_st16_nowait(a.ops + 16, wP + 16);
+    tmem_st16_nowait(a.ops + T / 2, wPB);
+    tmem_st16_nowait(a.ops + T / 2 + 16, wPB + 16);
+    s.publish_ops();
+    return true;
+  }
+  __device__ static void epilogue(Row& w, const Params& p, const EpiArgs& e) {
+    float alpha = w.alpha, unused = 0.f;
+    if (!e.sum_rows(alpha, unused)) return;
+    const size_t ro = ((size_t)e.head * p.N + e.blk0 + e.r) * D;
+    const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
+#pragma unroll 1
+    for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+      float y[16], o[16];
+      tmem_ld16(e.tm + c0, y);
+      const float4* src = reinterpret_cast<const float4*>(p.O + ro + c0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = src[q];
+        o[4 * q] = fmaf(-alpha, v.x, y[4 * q]);
+        o[4 * q + 1] = fmaf(-alpha, v.y, y[4 * q + 1]);
+        o[4 * q + 2] = fmaf(-alpha, v.z, y[4 * q + 2]);
+        o[4 * q + 3] = fmaf(-alpha, v.w, y[4 * q + 3]);
+      }
+      store16(p.gdO + ro + c0, o);
     }
   }
 };
@@ -279,7 +423,7 @@ struct Pass1 {
 template <int D_>
 struct Pass2 {
   using Params = P2Params;
-  static constexpr int D = D_, DC = D / 64;
+  static constexpr int D = D_, DC = D / 64, T = kT;
   static constexpr bool kAllTmem = D == 64;        // V, UV also in TMEM; operands in TMEM
   static constexpr int TRES = kAllTmem ? 4 : 2;    // K, UK (, V, UV)
   static constexpr int RES = kAllTmem ? 0 : 2 * DC * kChunk;   // V, UV in shared memory
@@ -446,7 +590,9 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   P1Params p1;
   const int BH = a.BH, N = a.N;
   bool ok = make_bf16_map(&p1.mK, a.K, BH, N, D, kT) && make_bf16_map(&p1.mUK, a.UK, BH, N, D, kT) &&
-            make_bf16_map(&p1.mV, a.V, BH, N, D, kT) && make_bf16_map(&p1.mUV, a.UV, BH, N, D, kT);
+            make_bf16_map(&p1.mV, a.V, BH, N, D, kT) && make_bf16_map(&p1.mUV, a.UV, BH, N, D, kT) &&
+            make_bf16_map(&p1.mK64, a.K, BH, N, D, 64) && make_bf16_map(&p1.mUK64, a.UK, BH, N, D, 64) &&
+            make_bf16_map(&p1.mV64, a.V, BH, N, D, 64) && make_bf16_map(&p1.mUV64, a.UV, BH, N, D, 64);
   if (!ok) return cudaErrorInvalidValue;
   p1.Q = static_cast<const __nv_bfloat16*>(a.Q);
   p1.UQ = static_cast<const __nv_bfloat16*>(a.UQ);
@@ -464,9 +610,9 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   p1.stall = c.stall;
   const dim3 grid(N / kM, BH);
   // the Z kernel reads what the U1 kernel wrote (U1 in gQ, alpha and E)
-  cudaError_t e = launch<Pass1<D, kU1>>("bob_pass1_u1", p1, grid, s);
-  if (e == cudaSuccess) e = launch<Pass1<D, kZ>>("bob_pass1_z", p1, grid, s);
-  if (e == cudaSuccess) e = launch<Pass1<D, kY>>("bob_pass1_y", p1, grid, s);
+  cudaError_t e = launch<PassU1<D>>("bob_pass1_u1", p1, grid, s);
+  if (e == cudaSuccess) e = launch<PassZ<D>>("bob_pass1_z", p1, grid, s);
+  if (e == cudaSuccess) e = launch<PassY<D>>("bob_pass1_y", p1, grid, s);
   if (e != cudaSuccess) return e;
   P2Params p2;
   ok = make_bf16_map(&p2.mQ, a.Q, BH, N, D, kT) && make_bf16_map(&p2.mUQ, a.UQ, BH, N, D, kT) &&

@@ -24,7 +24,6 @@ namespace {
 
 using namespace tc;
 using tile::kM;
-using tile::kT;
 
 // ===========================================================================
 // first backward on the tile skeleton
@@ -42,48 +41,54 @@ struct DqParams {
 };
 
 // Row kernel: resident Q, dO in TMEM (A operands of the score MMAs); ring A
-// = K (read by dQ += dS K), ring B = V (read only by dP = dO V^T).  dS goes to
-// TMEM (TS MMA).  TMEM: dQ (d) | [S | dP] x 2 | dS halves (2 x 16) | Q, dO (d).
+// = K (read by dQ += dS K), ring B = V (read only by dP = dO V^T), 64 keys
+// per tile.  TMEM: dQ (d) | [S | dP] x 2 | Q, dO (d) and, at d = 64, the dS
+// halves (TS MMA); at d = 128 dS goes to shared memory (SS MMA).
 template <int D_>
 struct DqOp {
   using Params = DqParams;
-  static constexpr int D = D_, DC = D / 64;
+  static constexpr int D = D_, DC = D / 64, T = 64, BLK = T * 128;
   static constexpr int RES = 0, TRES = 2;
-  static constexpr int ACH = tile::kBlk, BCH = tile::kBlk;
+  static constexpr int ACH = BLK, BCH = BLK;
   static constexpr int SA = DC * ACH, SB = DC * BCH, SA_TX = SA, SB_TX = SB;
-  static constexpr int NSA = 8, NSB = 8;
-  static constexpr bool VEC = false, ROW_SUMS = false, TS = true;
-  static constexpr int VEC_OFF = 0, OPS = 0;
-  static constexpr int ACC = D, SCOLS = 64, NBUF = 2;   // [S | dP]
-  static constexpr int OP_HALF = 16, OP_COL = ACC + NBUF * SCOLS;
-  static constexpr int TRES_COL = OP_COL + 2 * OP_HALF;
-  static constexpr int SMEM = NSA * SA + NSB * SB;
+  static constexpr int NSA = D == 128 ? 5 : 8, NSB = NSA;
+  static constexpr bool VEC = false, ROW_SUMS = false, TS = D == 64;
+  static constexpr int VEC_OFF = 0;
+  static constexpr int OPS = TS ? 0 : 2 * tile::kChunk;  // dS, one [128][64] tile per half
+  static constexpr int ACC = D, SCOLS = 2 * T, NBUF = 2;   // [S | dP]
+  static constexpr int OP_HALF = T / 2, OP_COL = ACC + NBUF * SCOLS;
+  static constexpr int TRES_COL = OP_COL + (TS ? 2 * OP_HALF : 0);
+  static constexpr int SMEM = NSA * SA + NSB * SB + OPS;
   static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
   static_assert(SMEM + 1024 <= 232448, "shared memory budget");
 
   __device__ static const void* tres_src(const Params& p, int s) { return s == 0 ? (const void*)p.Q : (const void*)p.dO; }
   __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
   __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
-    for (int kc = 0; kc < DC; ++kc) tma_load_3d(st + kc * ACH, &p.mK, bar, kc * 64, t * tile::kT, head);
+    for (int kc = 0; kc < DC; ++kc) tma_load_3d(st + kc * ACH, &p.mK, bar, kc * 64, t * T, head);
   }
   __device__ static void load_b(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
-    for (int kc = 0; kc < DC; ++kc) tma_load_3d(st + kc * BCH, &p.mV, bar, kc * 64, t * tile::kT, head);
+    for (int kc = 0; kc < DC; ++kc) tma_load_3d(st + kc * BCH, &p.mV, bar, kc * 64, t * T, head);
   }
   __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t, uint32_t sa, uint32_t sb) {
-    const uint32_t i32 = idesc_bf16(tile::kM, 32, false, false);
+    const uint32_t i64 = idesc_bf16(tile::kM, T, false, false);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-      mma_ts_w(sc, tile::tres_a(tres, 0, D, k), tile::kmaj_lo(sa, ACH, 0, k), i32, k > 0);       // S = Q K^T
-      mma_ts_w(sc + 32, tile::tres_a(tres, 1, D, k), tile::kmaj_lo(sb, BCH, 0, k), i32, k > 0);  // dP = dO V^T
+      mma_ts_w(sc, tile::tres_a(tres, 0, D, k), tile::kmaj(sa, ACH, 0, k), i64, k > 0);      // S = Q K^T
+      mma_ts_w(sc + T, tile::tres_a(tres, 1, D, k), tile::kmaj(sb, BCH, 0, k), i64, k > 0);  // dP = dO V^T
     }
   }
   __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
     const uint32_t amn = desc_lo(sa, ACH);
     const uint32_t id = idesc_bf16(tile::kM, D, false, true);
 #pragma unroll
-    for (int kk = 0; kk < 2; ++kk)
-      mma_ts_w(tb, ops + h * OP_HALF + kk * 8, tile::mn_lo(amn, 0, kk), id,
-             (first && kk == 0) ? 0u : 1u);  // dQ += dS K
+    for (int kk = 0; kk < T / 16; ++kk) {  // dQ += dS K
+      const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+      if (TS)
+        mma_ts_w(tb, ops + h * OP_HALF + kk * 8, tile::mnmaj(amn, 0, kk), id, acc);
+      else
+        mma_ss_w(tb, tile::op64_lo(ops, 0, h, kk), tile::mnmaj(amn, 0, kk), id, acc);
+    }
   }
   struct Row {
     float nL, Di;
@@ -115,14 +120,14 @@ struct DqOp {
     w.Di = Di;
     w.nL = -p.L[vo] * tile::kLog2e;
   }
-  __device__ static bool ew_tile(Row& w, const Params& p, const tile::TileArgs& a, const tile::TileSync& s, int) {
+  __device__ static bool ew_tile(Row& w, const Params& p, const tile::TileArgs& a, const tile::TileSync& s, int r) {
     const float sc = p.tau * tile::kLog2e;
-    uint32_t wd[16];
+    uint32_t wd[T / 2];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < T / 16; ++q) {
       float S[16], dP[16];
-      tmem_ld16x2(a.sc + q * 16, a.sc + 32 + q * 16, S, dP);
-      if (q == 1) s.release_scores();
+      tmem_ld16x2(a.sc + q * 16, a.sc + T + q * 16, S, dP);
+      if (q == T / 16 - 1) s.release_scores();
 #pragma unroll
       for (int j = 0; j < 16; j += 2) {
         const float p0 = tile::ex2(fmaf(S[j], sc, w.nL)), p1 = tile::ex2(fmaf(S[j + 1], sc, w.nL));
@@ -130,7 +135,12 @@ struct DqOp {
       }
     }
     if (!s.acquire_ops()) return false;
-    tmem_st16_nowait(a.ops, wd);
+    if (TS) {
+      tmem_st16_nowait(a.ops, wd);
+      tmem_st16_nowait(a.ops + 16, wd + 16);
+    } else {
+      tile::write_op64(a.ops + a.h * tile::kChunk, (uint32_t)r, wd);
+    }
     s.publish_ops();
     return true;
   }
@@ -161,22 +171,22 @@ struct DkvParams {
 };
 
 // Column kernel: resident K, V in TMEM; ring A = [Q | dO] + (L, D) of the
-// tile.  P and dS go to TMEM (TS MMAs).  TMEM: dK, dV (2d) | [S^T | dP^T] x
-// NBUF | (P, dS) halves (2 x 32) | K, V (d); one score buffer at d = 128.
+// tile, 64 queries per tile.  P and dS go to shared memory (SS MMAs).
+// TMEM: dK, dV (2d) | [S^T | dP^T] x NBUF | K, V (d); one score buffer at d = 128.
 template <int D_>
 struct DkvOp {
   using Params = DkvParams;
-  static constexpr int D = D_, DC = D / 64;
+  static constexpr int D = D_, DC = D / 64, T = 64, BLK = T * 128;
   static constexpr int RES = 0, TRES = 2;
-  static constexpr int ACH = 2 * tile::kBlk, VEC_OFF = DC * ACH;
-  static constexpr int SA = DC * ACH + 1024, SA_TX = DC * ACH + 256, SB = 0, SB_TX = 0;
-  static constexpr int NSA = 8, NSB = 0;
-  static constexpr bool VEC = true, ROW_SUMS = false, TS = true;
-  static constexpr int OPS = 0;
-  static constexpr int ACC = 2 * D, SCOLS = 64, NBUF = D == 128 ? 1 : 2;   // dK, dV; [S^T | dP^T]
-  static constexpr int OP_HALF = 32, OP_COL = ACC + NBUF * SCOLS;
-  static constexpr int TRES_COL = OP_COL + 2 * OP_HALF;
-  static constexpr int SMEM = NSA * SA;
+  static constexpr int ACH = 2 * BLK, VEC_OFF = DC * ACH;
+  static constexpr int SA = DC * ACH + 1024, SA_TX = DC * ACH + 2 * T * 4, SB = 0, SB_TX = 0;
+  static constexpr int NSA = D == 128 ? 4 : 8, NSB = 0;
+  static constexpr bool VEC = true, ROW_SUMS = false, TS = false;
+  static constexpr int OPS = 4 * tile::kChunk;   // P, dS: one [128][64] tile per operand and half
+  static constexpr int ACC = 2 * D, SCOLS = 2 * T, NBUF = D == 128 ? 1 : 2;   // dK, dV; [S^T | dP^T]
+  static constexpr int OP_HALF = 0, OP_COL = ACC + NBUF * SCOLS;
+  static constexpr int TRES_COL = OP_COL;
+  static constexpr int SMEM = NSA * SA + OPS;
   static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
   static_assert(SMEM + 1024 <= 232448, "shared memory budget");
 
@@ -184,45 +194,44 @@ struct DkvOp {
   __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
   __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
     for (int kc = 0; kc < DC; ++kc) {
-      tma_load_3d(st + kc * ACH, &p.mQ, bar, kc * 64, t * tile::kT, head);
-      tma_load_3d(st + kc * ACH + tile::kBlk, &p.mdO, bar, kc * 64, t * tile::kT, head);
+      tma_load_3d(st + kc * ACH, &p.mQ, bar, kc * 64, t * T, head);
+      tma_load_3d(st + kc * ACH + BLK, &p.mdO, bar, kc * 64, t * T, head);
     }
-    const size_t v = (size_t)head * p.N + (size_t)t * tile::kT;
-    tile::bulk_load(st + VEC_OFF, p.L + v, 128, bar);
-    tile::bulk_load(st + VEC_OFF + 128, p.D + v, 128, bar);
+    const size_t v = (size_t)head * p.N + (size_t)t * T;
+    tile::bulk_load(st + VEC_OFF, p.L + v, T * 4, bar);
+    tile::bulk_load(st + VEC_OFF + T * 4, p.D + v, T * 4, bar);
   }
   __device__ static void load_b(const Params&, uint8_t*, uint64_t*, int, int) {}
   __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t, uint32_t sa, uint32_t) {
-    const uint32_t i32 = idesc_bf16(tile::kM, 32, false, false);
+    const uint32_t i64 = idesc_bf16(tile::kM, T, false, false);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-      mma_ts_w(sc, tile::tres_a(tres, 0, D, k), tile::kmaj_lo(sa, ACH, 0, k), i32, k > 0);       // S^T = K Q^T
-      mma_ts_w(sc + 32, tile::tres_a(tres, 1, D, k), tile::kmaj_lo(sa, ACH, 1, k), i32, k > 0);  // dP^T = V dO^T
+      mma_ts_w(sc, tile::tres_a(tres, 0, D, k), tile::kmaj(sa, ACH, 0, k), i64, k > 0);        // S^T = K Q^T
+      mma_ts_w(sc + T, tile::tres_a(tres, 1, D, k), tile::kmaj(sa, ACH, BLK, k), i64, k > 0);  // dP^T = V dO^T
     }
   }
   __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
     const uint32_t amn = desc_lo(sa, ACH);
     const uint32_t id = idesc_bf16(tile::kM, D, false, true);
 #pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
-      const uint32_t a = ops + h * OP_HALF + kk * 8;
-      mma_ts_w(tb + D, a, tile::mn_lo(amn, 1, kk), id, acc0);   // dV += P^T dO
-      mma_ts_w(tb, a + 16, tile::mn_lo(amn, 0, kk), id, acc0);  // dK += dS^T Q
+    for (int kk = 0; kk < T / 16; ++kk) {
+      const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+      mma_ss_w(tb + D, tile::op64_lo(ops, 0, h, kk), tile::mnmaj(amn, BLK, kk), id, acc);  // dV += P^T dO
+      mma_ss_w(tb, tile::op64_lo(ops, 1, h, kk), tile::mnmaj(amn, 0, kk), id, acc);        // dK += dS^T Q
     }
   }
   struct Row {};
   __device__ static void ew_init(Row&, const Params&, int, int, int) {}
-  __device__ static bool ew_tile(Row&, const Params& p, const tile::TileArgs& a, const tile::TileSync& s, int) {
+  __device__ static bool ew_tile(Row&, const Params& p, const tile::TileArgs& a, const tile::TileSync& s, int r) {
     const float sc = p.tau * tile::kLog2e;
     const float* vL = a.vec;
-    const float* vD = a.vec + 32;
-    uint32_t wP[16], wd[16];
+    const float* vD = a.vec + T;
+    uint32_t wP[T / 2], wd[T / 2];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < T / 16; ++q) {
       float S[16], dP[16];
-      tmem_ld16x2(a.sc + q * 16, a.sc + 32 + q * 16, S, dP);
-      if (q == 1) s.release_scores();
+      tmem_ld16x2(a.sc + q * 16, a.sc + T + q * 16, S, dP);
+      if (q == T / 16 - 1) s.release_scores();
 #pragma unroll
       for (int c = 0; c < 16; c += 2) {
         const int ii = q * 16 + c;
@@ -233,8 +242,8 @@ struct DkvOp {
       }
     }
     if (!s.acquire_ops()) return false;
-    tmem_st16_nowait(a.ops, wP);
-    tmem_st16_nowait(a.ops + 16, wd);
+    tile::write_op64(a.ops + a.h * tile::kChunk, (uint32_t)r, wP);
+    tile::write_op64(a.ops + (2 + a.h) * tile::kChunk, (uint32_t)r, wd);
     s.publish_ops();
     return true;
   }
@@ -269,7 +278,7 @@ cudaError_t launch(const char* name, K kernel, int smem, int threads, dim3 grid,
 template <int D>
 cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
   DqParams q;
-  if (!make_bf16_map(&q.mK, a.K, a.BH, a.N, D, kT) || !make_bf16_map(&q.mV, a.V, a.BH, a.N, D, kT))
+  if (!make_bf16_map(&q.mK, a.K, a.BH, a.N, D, DqOp<D>::T) || !make_bf16_map(&q.mV, a.V, a.BH, a.N, D, DqOp<D>::T))
     return cudaErrorInvalidValue;
   q.Q = static_cast<const __nv_bfloat16*>(a.Q);
   q.O = a.O;
@@ -286,7 +295,7 @@ cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
   cudaError_t e = launch("attn_bwd_dq", tile::tile_kernel<DqOp<D>>, DqOp<D>::SMEM, tile::kThreads, grid, q, s);
   if (e != cudaSuccess) return e;
   DkvParams k;
-  if (!make_bf16_map(&k.mQ, a.Q, a.BH, a.N, D, kT) || !make_bf16_map(&k.mdO, a.dO, a.BH, a.N, D, kT))
+  if (!make_bf16_map(&k.mQ, a.Q, a.BH, a.N, D, DkvOp<D>::T) || !make_bf16_map(&k.mdO, a.dO, a.BH, a.N, D, DkvOp<D>::T))
     return cudaErrorInvalidValue;
   k.K = static_cast<const __nv_bfloat16*>(a.K);
   k.V = static_cast<const __nv_bfloat16*>(a.V);

@@ -20,7 +20,7 @@
 // the 32- and 64-column score MMAs off the shared-memory bandwidth limit.
 // Residents the policy keeps in shared memory (RES > 0) arrive by TMA.
 //
-// Per 32-row streamed tile t:
+// Per streamed tile t (Op::T = 32 or 64 rows):
 //   1. TMA fills ring A (operands the accumulator MMAs also read, plus any
 //      per-tile vectors) and ring B (operands only the score MMAs read); both
 //      stages of a tile complete one barrier.
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
   __shared__ Ctrl ctrl;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int blk0 = blockIdx.x * kM, head = blockIdx.y;
-  const int nt = p.N / kT;
+  const int nt = p.N / Op::T;
   uint8_t* res = smem;
   uint8_t* ring_a = res + Op::RES;
   uint8_t* ring_b = ring_a + Op::NSA * Op::SA;
@@ -424,6 +424,26 @@ __device__ __forceinline__ uint32_t mn_lo(uint32_t st_mn_lo0, int blk, int kk) {
 // K-major operand tile `slot` ([128][64], 16 KB each), half h, kk-th 16-column step.
 __device__ __forceinline__ uint32_t op_lo(uint32_t ops_lo0, int slot, uint32_t h, int kk) {
   return ops_lo0 + (uint32_t)((slot * kChunk + kk * 32) >> 4) + h * 4u;
+}
+
+// Byte-offset forms for any streamed tile height: `off` is the byte offset
+// of the operand block inside a 64-column chunk (block b of T rows: b * T * 128).
+__device__ __forceinline__ uint32_t kmaj(uint32_t st_lo0, int chunk, int off, int k) {
+  return st_lo0 + (uint32_t)(((k >> 2) * chunk + off + (k & 3) * 32) >> 4);
+}
+__device__ __forceinline__ uint32_t mnmaj(uint32_t st_mn_lo0, int off, int kk) {
+  return st_mn_lo0 + (uint32_t)((off + kk * 2048) >> 4);
+}
+// 64-row tiles: operand `slot` of half h is its own [128][64] tile
+// ((2 slot + h)-th 16 KB tile), kk-th 16-column step.
+__device__ __forceinline__ uint32_t op64_lo(uint32_t ops_lo0, int slot, uint32_t h, int kk) {
+  return ops_lo0 + (uint32_t)(((2 * slot + (int)h) * kChunk + kk * 32) >> 4);
+}
+// Write 64 packed bf16 (32 words) of row r into a 128B-swizzled [128][64] tile.
+__device__ __forceinline__ void write_op64(uint32_t tile, uint32_t r, const uint32_t* w) {
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc)
+    st_shared_v4(tile + sw128_offset(r, cc), w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
 }
 
 // Write 32 packed bf16 (16 words) of row r into columns [32h, 32h+32) of a
