@@ -55,6 +55,7 @@ using namespace tile;
 struct P1Params {
   CUtensorMap mK, mUK, mV, mUV;              // streamed, box {64, 32} (U1 sweep)
   CUtensorMap mK64, mUK64, mV64, mUV64;      // streamed, box {64, 64} (Z and Y sweeps)
+  CUtensorMap mdO_res;                       // resident, box {64, 128} (U1 sweep at d = 128)
   const __nv_bfloat16 *Q, *UQ, *dO;          // resident (copied into TMEM)
   const float *L, *D, *O;
   float *gQ, *gdO, *ws;
@@ -90,37 +91,43 @@ __device__ __forceinline__ void load_tile2(const CUtensorMap* m0, const CUtensor
 }
 
 // U1 sweep (32 keys per tile): U1 += dS UK + X K, alpha, EX.  Ring A = [K UK]
-// (also read by the accumulator MMAs), ring B = [V UV].
+// (also read by the accumulator MMAs), ring B = [V UV].  At d = 64 Q, UQ, dO
+// and the dS, X operands sit in TMEM; at d = 128 dO and the operands move to
+// shared memory, which leaves TMEM room for two score buffers.
 template <int D_>
 struct PassU1 {
   using Params = P1Params;
   static constexpr int D = D_, DC = D / 64, T = 32;
-  static constexpr int RES = 0, TRES = 3;   // Q, UQ, dO
+  static constexpr bool kWide = D == 128;
+  static constexpr int TRES = kWide ? 2 : 3;            // Q, UQ (, dO)
+  static constexpr int RES = kWide ? DC * kChunk : 0;   // dO in shared memory
   static constexpr int ACH = 2 * kBlk, BCH = 2 * kBlk;
   static constexpr int SA = DC * ACH, SB = DC * BCH, SA_TX = SA, SB_TX = SB;
-  static constexpr int NSA = D == 128 ? 6 : 8, NSB = NSA;
-  static constexpr bool VEC = false, ROW_SUMS = true, TS = true;
-  static constexpr int VEC_OFF = 0, OPS = 0;
-  static constexpr int ACC = D, SCOLS = 128;           // [S|B|dP|C]
-  static constexpr int NBUF = D == 128 ? 1 : 2;
-  static constexpr int OP_HALF = 32;                    // dS, X
+  static constexpr int NSA = kWide ? 5 : 8, NSB = NSA;
+  static constexpr bool VEC = false, ROW_SUMS = true, TS = !kWide;
+  static constexpr int VEC_OFF = 0;
+  static constexpr int OPS = kWide ? 2 * kChunk : 0;    // dS, X tiles; half h = columns 32h..32h+31
+  static constexpr int ACC = D, SCOLS = 128, NBUF = 2;  // [S|B|dP|C]
+  static constexpr int OP_HALF = 32;                    // TMEM operands dS, X
   static constexpr int OP_COL = ACC + NBUF * SCOLS;
-  static constexpr int TRES_COL = OP_COL + 2 * OP_HALF;
-  static constexpr int SMEM = NSA * SA + NSB * SB;
+  static constexpr int TRES_COL = OP_COL + (TS ? 2 * OP_HALF : 0);
+  static constexpr int SMEM = RES + NSA * SA + NSB * SB + OPS;
   static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
   static_assert(SMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
 
   __device__ static const void* tres_src(const Params& p, int s) {
     return s == 0 ? (const void*)p.Q : s == 1 ? (const void*)p.UQ : (const void*)p.dO;
   }
-  __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
+  __device__ static void load_res(const Params& p, uint8_t* res, uint64_t* bar, int row0, int head) {
+    for (int kc = 0; kc < DC; ++kc) tma_load_3d(res + kc * kChunk, &p.mdO_res, bar, kc * 64, row0, head);
+  }
   __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
     load_tile2(&p.mK, &p.mUK, st, DC, ACH, kBlk, bar, t * T, head);
   }
   __device__ static void load_b(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
     load_tile2(&p.mV, &p.mUV, st, DC, BCH, kBlk, bar, t * T, head);
   }
-  __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t, uint32_t sa, uint32_t sb) {
+  __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t res, uint32_t sa, uint32_t sb) {
     const uint32_t i64 = idesc_bf16(kM, 64, false, false), i32 = idesc_bf16(kM, 32, false, false);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k)  // [S | Q UK^T] = Q [K; UK]^T
@@ -129,17 +136,27 @@ struct PassU1 {
     for (int k = 0; k < D / 16; ++k)  // B += UQ K^T
       mma_ts_w(sc + 32, tres_a(tres, 1, D, k), kmaj(sa, ACH, 0, k), i32, 1);
 #pragma unroll
-    for (int k = 0; k < D / 16; ++k)  // [dP | C] = dO [V; UV]^T
-      mma_ts_w(sc + 64, tres_a(tres, 2, D, k), kmaj(sb, BCH, 0, k), i64, k > 0);
+    for (int k = 0; k < D / 16; ++k) {  // [dP | C] = dO [V; UV]^T
+      if (kWide)
+        mma_ss_w(sc + 64, res_lo(res, 0, DC, k), kmaj(sb, BCH, 0, k), i64, k > 0);
+      else
+        mma_ts_w(sc + 64, tres_a(tres, 2, D, k), kmaj(sb, BCH, 0, k), i64, k > 0);
+    }
   }
   __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
     const uint32_t amn = desc_lo(sa, ACH);
     const uint32_t id = idesc_bf16(kM, D, false, true);
 #pragma unroll
     for (int kk = 0; kk < T / 16; ++kk) {
-      const uint32_t a = ops + h * OP_HALF + kk * 8;
-      mma_ts_w(tb, a, mnmaj(amn, kBlk, kk), id, (first && kk == 0) ? 0u : 1u);  // U1 += dS UK
-      mma_ts_w(tb, a + 16, mnmaj(amn, 0, kk), id, 1);                            // U1 += X K
+      const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
+      if (kWide) {
+        mma_ss_w(tb, op_lo(ops, 0, h, kk), mnmaj(amn, kBlk, kk), id, acc0);  // U1 += dS UK
+        mma_ss_w(tb, op_lo(ops, 1, h, kk), mnmaj(amn, 0, kk), id, 1);        // U1 += X K
+      } else {
+        const uint32_t a = ops + h * OP_HALF + kk * 8;
+        mma_ts_w(tb, a, mnmaj(amn, kBlk, kk), id, acc0);
+        mma_ts_w(tb, a + 16, mnmaj(amn, 0, kk), id, 1);
+      }
     }
   }
   struct Row {
@@ -152,7 +169,7 @@ struct PassU1 {
     w.alpha = 0.f;
     w.ex = 0.f;
   }
-  __device__ static bool ew_tile(Row& w, const Params& p, const TileArgs& a, const TileSync& s, int) {
+  __device__ static bool ew_tile(Row& w, const Params& p, const TileArgs& a, const TileSync& s, int r) {
     const float sc = p.tau * kLog2e;
     uint32_t wdS[16], wX[16];
 #pragma unroll
@@ -178,8 +195,13 @@ struct PassU1 {
       }
     }
     if (!s.acquire_ops()) return false;
-    tmem_st16_nowait(a.ops, wdS);
-    tmem_st16_nowait(a.ops + 16, wX);
+    if (kWide) {
+      write_op_half(a.ops, (uint32_t)r, a.h, wdS);
+      write_op_half(a.ops + kChunk, (uint32_t)r, a.h, wX);
+    } else {
+      tmem_st16_nowait(a.ops, wdS);
+      tmem_st16_nowait(a.ops + 16, wX);
+    }
     s.publish_ops();
     return true;
   }
@@ -310,20 +332,20 @@ struct PassZ {
   }
 };
 
-// Y sweep (64 keys per tile): Y += P UV + PB V, alpha; gdO = Y - alpha O.
-// Ring A = [V UV] (read by the accumulator MMAs), ring B = [K UK].  P and PB
-// go to TMEM; one score buffer at d = 128.
+// Y sweep: Y += P UV + PB V, alpha; gdO = Y - alpha O.  Ring A = [V UV]
+// (read by the accumulator MMAs), ring B = [K UK].  P and PB go to TMEM; 64
+// keys per tile at d = 64, 32 at d = 128 (two score buffers either way).
 template <int D_>
 struct PassY {
   using Params = P1Params;
-  static constexpr int D = D_, DC = D / 64, T = 64, BLK = T * 128;
+  static constexpr int D = D_, DC = D / 64, T = D == 128 ? 32 : 64, BLK = T * 128;
   static constexpr int RES = 0, TRES = 2;   // Q, UQ
   static constexpr int ACH = 2 * BLK, BCH = 2 * BLK;
   static constexpr int SA = DC * ACH, SB = DC * BCH, SA_TX = SA, SB_TX = SB;
-  static constexpr int NSA = D == 128 ? 3 : 6, NSB = NSA;
+  static constexpr int NSA = 6, NSB = NSA;
   static constexpr bool VEC = false, ROW_SUMS = true, TS = true;
   static constexpr int VEC_OFF = 0, OPS = 0;
-  static constexpr int ACC = D, SCOLS = 2 * T, NBUF = D == 128 ? 1 : 2;   // [S | B]
+  static constexpr int ACC = D, SCOLS = 2 * T, NBUF = 2;   // [S | B]
   static constexpr int OP_HALF = T;                     // P, PB (32 columns each)
   static constexpr int OP_COL = ACC + NBUF * SCOLS;
   static constexpr int TRES_COL = OP_COL + 2 * OP_HALF;
@@ -334,10 +356,10 @@ struct PassY {
   __device__ static const void* tres_src(const Params& p, int s) { return s == 0 ? (const void*)p.Q : (const void*)p.UQ; }
   __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
   __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
-    load_tile2(&p.mV64, &p.mUV64, st, DC, ACH, BLK, bar, t * T, head);
+    load_tile2(T == 64 ? &p.mV64 : &p.mV, T == 64 ? &p.mUV64 : &p.mUV, st, DC, ACH, BLK, bar, t * T, head);
   }
   __device__ static void load_b(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
-    load_tile2(&p.mK64, &p.mUK64, st, DC, BCH, BLK, bar, t * T, head);
+    load_tile2(T == 64 ? &p.mK64 : &p.mK, T == 64 ? &p.mUK64 : &p.mUK, st, DC, BCH, BLK, bar, t * T, head);
   }
   __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t, uint32_t, uint32_t sb) {
     const uint32_t i128 = idesc_bf16(kM, 2 * T, false, false), i64 = idesc_bf16(kM, T, false, false);
@@ -387,10 +409,11 @@ struct PassY {
       }
     }
     if (!s.acquire_ops()) return false;
-    tmem_st16_nowait(a.ops, wP);
-    tmem_st16_nowait(a.ops + 16, wP + 16);
-    tmem_st16_nowait(a.ops + T / 2, wPB);
-    tmem_st16_nowait(a.ops + T / 2 + 16, wPB + 16);
+#pragma unroll
+    for (int c = 0; c < T / 32; ++c) {
+      tmem_st16_nowait(a.ops + 16 * c, wP + 16 * c);
+      tmem_st16_nowait(a.ops + T / 2 + 16 * c, wPB + 16 * c);
+    }
     s.publish_ops();
     return true;
   }
@@ -592,7 +615,8 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   bool ok = make_bf16_map(&p1.mK, a.K, BH, N, D, kT) && make_bf16_map(&p1.mUK, a.UK, BH, N, D, kT) &&
             make_bf16_map(&p1.mV, a.V, BH, N, D, kT) && make_bf16_map(&p1.mUV, a.UV, BH, N, D, kT) &&
             make_bf16_map(&p1.mK64, a.K, BH, N, D, 64) && make_bf16_map(&p1.mUK64, a.UK, BH, N, D, 64) &&
-            make_bf16_map(&p1.mV64, a.V, BH, N, D, 64) && make_bf16_map(&p1.mUV64, a.UV, BH, N, D, 64);
+            make_bf16_map(&p1.mV64, a.V, BH, N, D, 64) && make_bf16_map(&p1.mUV64, a.UV, BH, N, D, 64) &&
+            make_bf16_map(&p1.mdO_res, a.dO, BH, N, D, kM);
   if (!ok) return cudaErrorInvalidValue;
   p1.Q = static_cast<const __nv_bfloat16*>(a.Q);
   p1.UQ = static_cast<const __nv_bfloat16*>(a.UQ);

@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
   const Waiter wt{&ctrl.abort_flag, p.err, p.wait_ns};
   const bool live = ctrl.abort_flag == 0;
 #ifdef FBOB_TRACE
-  constexpr int kTraceId = Op::ACC * 1000000 + Op::SCOLS * 1000 + Op::TRES * 100 + Op::OP_HALF;
+  constexpr int kTraceId = Op::ACC * 1000000 + Op::SCOLS * 1000 + Op::TRES * 100 + Op::OP_HALF / 16 * 10 + Op::T / 32;
   const bool trace_cta = blockIdx.x == 0 && blockIdx.y == 0 && g_trace_sel == kTraceId && (tid & 31) == 0;
   const bool trace_on = trace_cta && (warp >= kEwWarps || (warp & 3) == 0);
 #endif
