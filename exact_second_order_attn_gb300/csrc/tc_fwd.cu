@@ -3,17 +3,19 @@
 // natural-log row logsumexp L (FlashBoB abstract: the FlashAttention-style
 // forward whose outputs the first backward and BoB consume).
 //
-// A CTA owns two 128-row query blocks (A, B) that share every streamed
-// 32-key tile of K and V.  Ten warps: warpgroup 0 (warps 0-3) runs the
-// online softmax of block A, warpgroup 1 (warps 4-7) that of block B (thread
-// r = TMEM lane r = row r of its block, so row max / sum are thread-local),
-// warp 8 issues TMA, warp 9 issues tcgen05.mma and owns TMEM.
-// Per tile t and block X:  S_X = Q_X K_t^T (fp32, TMEM);  the group computes
-// P = 2^(x - m) with x = tau log2(e) S and its running max m, writes P as bf16
-// into TMEM;  O_X += P V_t (A operand from TMEM).  The running max moves only
-// when a row's tile max exceeds it by more than 8 (lazy rescale), so P <= 2^8
-// stays well inside bf16 and O_X is rescaled in TMEM only then (after the
-// group's previous P V product has landed).  O = O_X / l, L = (m + log2 l) ln 2.
+// A CTA owns two 128-row query blocks (A, B) and streams K and V in tiles of
+// 128 keys.  TMEM: O_A, O_B (d columns each), S_A, S_B (128 columns each: 512
+// in all at d = 128).  Per tile t and block X:
+//   S_X = Q_X K_t^T         one SS MMA of N = 128 (issued by warp 9);
+//   softmax (warpgroup X, thread r = row r): two passes over S_X - the row
+//     max, then P = 2^(x - m) with x = tau log2(e) S - written as bf16 over
+//     the first 64 columns of S_X;
+//   O_X += P V_t            TS MMA, P read from TMEM (issued by warp 10).
+// Because P overwrites S, S_X(t+1) is issued only after O_X += P V_t has
+// completed.  The running max moves only when a row's tile max exceeds it by
+// more than 8 (lazy rescale), so P <= 2^8 stays well inside bf16 and O_X is
+// rescaled in TMEM only then (after the previous P V product has landed).
+// O = O_X / l, L = (m + log2 l) ln 2.  Warp 8 issues TMA.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -27,21 +29,18 @@ namespace fbob {
 namespace {
 
 using namespace tc;
-using tile::kBlk;
 using tile::kChunk;
 using tile::kLog2e;
 using tile::kM;
-using tile::kT;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
+constexpr int kKT = 128;                  // keys per tile
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescale = 8.0f;          // lazy-rescale threshold (log2 units)
 constexpr uint64_t kDrainNs = 200000000ull;
-constexpr int kNS = 6;                    // K/V stages
 
 struct FwdParams {
-  CUtensorMap mQ;          // resident, box {64, 128}
-  CUtensorMap mK, mV;      // streamed, box {64, 32}
+  CUtensorMap mQ, mK, mV;  // box {64, 128}
   float *O, *L;
   int N;
   float tau;
@@ -53,57 +52,52 @@ struct FwdParams {
 template <int D>
 struct FwdCfg {
   static constexpr int DC = D / 64;
-  static constexpr int RES = 2 * DC * kChunk;    // Q of blocks A and B
-  static constexpr int CH = 2 * kBlk;            // [K(32) | V(32)] per 64-column chunk
-  static constexpr int STAGE = DC * CH;
-  static constexpr int SMEM = RES + kNS * STAGE;
-  // TMEM: O_A, O_B, then per block two 32-column S buffers, then per block two
-  // 16-column P halves
-  static constexpr int S_COL = 2 * D, P_COL = 2 * D + 128;
-  static_assert(P_COL + 64 <= 512, "TMEM budget");
+  static constexpr int TILE = DC * kChunk;       // one 128 x d tile (Q block, K or V tile)
+  static constexpr int NK = D == 128 ? 3 : 4, NV = D == 128 ? 2 : 4;
+  static constexpr int Q_OFF = 0, K_OFF = 2 * TILE, V_OFF = K_OFF + NK * TILE;
+  static constexpr int SMEM = V_OFF + NV * TILE;
+  static constexpr int S_COL = 2 * D;            // S_A at S_COL, S_B at S_COL + 128
+  static_assert(S_COL + 2 * kKT <= 512, "TMEM budget");
   static_assert(SMEM + 1024 <= 232448, "shared memory budget");
 };
 
 struct Ctrl {
-  uint64_t res_full;
-  uint64_t st_full[kNS], st_empty[kNS];
-  uint64_t s_full[2][2], s_empty[2][2];   // [block][buffer]
-  uint64_t o_full[2][2], o_empty[2][2];   // [block][P half]
-  uint64_t acc_full[2];
-  uint64_t drain;
+  uint64_t q_full;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2], o_done[2];   // per block
+  uint64_t drain_s, drain_p;
   uint32_t tmem_base;
   int abort_flag;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) attn_fwd2_tc(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ Ctrl ctrl;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int row0 = blockIdx.x * 2 * kM, head = blockIdx.y;
   const int nblk = (row0 + kM < p.N) ? 2 : 1;   // block B exists unless N is an odd multiple of 128
-  const int nt = p.N / kT;
-  uint8_t* res = smem;
-  uint8_t* stages = res + C::RES;
+  const int nt = p.N / kKT;
 
   if (tid == 0) {
     ctrl.abort_flag = 0;
-    mbar_init(&ctrl.res_full, 1);
-    for (int s = 0; s < kNS; ++s) {
-      mbar_init(&ctrl.st_full[s], 1);
-      mbar_init(&ctrl.st_empty[s], nblk);   // one P V commit per block
+    mbar_init(&ctrl.q_full, 1);
+    for (int s = 0; s < C::NK; ++s) {
+      mbar_init(&ctrl.k_full[s], 1);
+      mbar_init(&ctrl.k_empty[s], 1);
     }
-    for (int x = 0; x < 2; ++x)
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(&ctrl.s_full[x][b], 1);
-        mbar_init(&ctrl.s_empty[x][b], 128);
-        mbar_init(&ctrl.o_full[x][b], 128);
-        mbar_init(&ctrl.o_empty[x][b], 1);
-      }
-    mbar_init(&ctrl.acc_full[0], 1);
-    mbar_init(&ctrl.acc_full[1], 1);
-    mbar_init(&ctrl.drain, 1);
+    for (int s = 0; s < C::NV; ++s) {
+      mbar_init(&ctrl.v_full[s], 1);
+      mbar_init(&ctrl.v_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&ctrl.s_full[x], 1);
+      mbar_init(&ctrl.p_full[x], 128);
+      mbar_init(&ctrl.o_done[x], 1);
+    }
+    mbar_init(&ctrl.drain_s, 1);
+    mbar_init(&ctrl.drain_p, 1);
     fence_mbar_init();
     if ((smem_u32(smem) & 1023u) != 0u) {
       ctrl.abort_flag = 1;
@@ -120,136 +114,121 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd2_tc(const __grid_constan
   const uint32_t tb = ctrl.tmem_base;
   const Waiter wt{&ctrl.abort_flag, p.err, p.wait_ns};
   const bool live = ctrl.abort_flag == 0;
+  const uint32_t sm0 = smem_u32(smem);
 
   if (warp == 8) {
     // ------------------------------------------------------------------ TMA
     if (live && (tid & 31) == 0) {
-      int issued = 0;
-      mbar_arrive_expect_tx(&ctrl.res_full, nblk * C::DC * kChunk);
+      mbar_arrive_expect_tx(&ctrl.q_full, nblk * C::TILE);
       for (int x = 0; x < nblk; ++x)
         for (int kc = 0; kc < C::DC; ++kc)
-          tma_load_3d(res + (x * C::DC + kc) * kChunk, &p.mQ, &ctrl.res_full, kc * 64, row0 + x * kM, head);
+          tma_load_3d(smem + C::Q_OFF + x * C::TILE + kc * kChunk, &p.mQ, &ctrl.q_full, kc * 64, row0 + x * kM, head);
+      int ik = 0, iv = 0;
       bool ok = true;
+      // K runs up to NK tiles ahead, V up to NV; K(t) is issued before V(t)
       for (int t = 0; t < nt && ok; ++t) {
-        const int s = t % kNS;
-        if (!(ok = mbar_wait(&ctrl.st_empty[s], ((t / kNS) & 1) ^ 1, wt))) break;
-        if (p.stall && t == 0) continue;  // test hook: nothing will fill this stage
-        mbar_arrive_expect_tx(&ctrl.st_full[s], C::STAGE);
-        uint8_t* st = stages + s * C::STAGE;
-        for (int kc = 0; kc < C::DC; ++kc) {
-          tma_load_3d(st + kc * C::CH, &p.mK, &ctrl.st_full[s], kc * 64, t * kT, head);
-          tma_load_3d(st + kc * C::CH + kBlk, &p.mV, &ctrl.st_full[s], kc * 64, t * kT, head);
+        const int sk = t % C::NK, sv = t % C::NV;
+        if (!(ok = mbar_wait(&ctrl.k_empty[sk], ((t / C::NK) & 1) ^ 1, wt))) break;
+        if (!(p.stall && t == 0)) {  // test hook: nothing fills the first K stage
+          mbar_arrive_expect_tx(&ctrl.k_full[sk], C::TILE);
+          for (int kc = 0; kc < C::DC; ++kc)
+            tma_load_3d(smem + C::K_OFF + sk * C::TILE + kc * kChunk, &p.mK, &ctrl.k_full[sk], kc * 64, t * kKT, head);
+          ik = t + 1;
         }
-        issued = t + 1;
+        if (!(ok = mbar_wait(&ctrl.v_empty[sv], ((t / C::NV) & 1) ^ 1, wt))) break;
+        mbar_arrive_expect_tx(&ctrl.v_full[sv], C::TILE);
+        for (int kc = 0; kc < C::DC; ++kc)
+          tma_load_3d(smem + C::V_OFF + sv * C::TILE + kc * kChunk, &p.mV, &ctrl.v_full[sv], kc * 64, t * kKT, head);
+        iv = t + 1;
       }
       if (!ok) {
-        mbar_wait_drain(&ctrl.res_full, 0, kDrainNs);
-        for (int t = (issued > kNS ? issued - kNS : 0); t < issued; ++t)
-          mbar_wait_drain(&ctrl.st_full[t % kNS], (t / kNS) & 1, kDrainNs);
+        // give-up path: every copy already issued lands before the CTA exits
+        mbar_wait_drain(&ctrl.q_full, 0, kDrainNs);
+        for (int t = (ik > C::NK ? ik - C::NK : 0); t < ik; ++t)
+          mbar_wait_drain(&ctrl.k_full[t % C::NK], (t / C::NK) & 1, kDrainNs);
+        for (int t = (iv > C::NV ? iv - C::NV : 0); t < iv; ++t)
+          mbar_wait_drain(&ctrl.v_full[t % C::NV], (t / C::NV) & 1, kDrainNs);
       }
     }
   } else if (warp == 9) {
-    // ------------------------------------------------------------------ MMA
-    // S(t) for both blocks, and P V per block, each issued in order; the
-    // warp issues whatever is ready (P V first), probing without blocking.
+    // ------------------------------------------------------- S = Q K^T MMAs
+    // S_X(t) waits for K(t) and, for t > 0, for O_X += P V_{t-1} to have
+    // completed (P_X(t-1) lives in S_X's columns).
     if (live) {  // the whole warp runs the loop; lane 0 issues (elect.sync)
-      const uint32_t res_l = desc_lo(smem_u32(res), 16), st_a = smem_u32(stages);
-      const uint32_t i32 = idesc_bf16(kM, 32, false, false);
-      const uint32_t id = idesc_bf16(kM, D, false, true);
-      bool ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.res_full, 0, wt));
-      int ns = 0, na[2] = {0, nblk > 1 ? 0 : nt};
-      uint64_t idle_since = 0;
-      uint32_t idle = 0;  // empty polls since the last check of the clock
-      while (ok && (na[0] < nt || na[1] < nt)) {
-        bool progressed = false;
-        for (int x = 0; x < nblk; ++x) {
-          const int u = na[x];
-          if (u < ns && mbar_test_w(&ctrl.o_full[x][u & 1], (u >> 1) & 1)) {
-            tc_fence_after();
-            const uint32_t vmn = desc_lo(st_a + (u % kNS) * C::STAGE, C::CH);
+      const uint32_t q_lo = desc_lo(sm0 + C::Q_OFF, 16);
+      const uint32_t i128 = idesc_bf16(kM, kKT, false, false);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.q_full, 0, wt));
+      for (int t = 0; ok && t < nt; ++t) {
+        const int sk = t % C::NK;
+        const uint32_t k_lo = desc_lo(sm0 + C::K_OFF + sk * C::TILE, 16);
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.k_full[sk], (t / C::NK) & 1, wt));
+        for (int x = 0; ok && x < nblk; ++x) {
+          if (t > 0) ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.o_done[x], (t - 1) & 1, wt));
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
-              mma_ts_w(tb + x * D, tb + C::P_COL + x * 32 + (u & 1) * 16 + kk * 8, tile::mn_lo(vmn, 1, kk), id,
-                        (u == 0 && kk == 0) ? 0u : 1u);
-            mma_commit_w(&ctrl.o_empty[x][u & 1]);
-            mma_commit_w(&ctrl.st_empty[u % kNS]);
-            if (u + 1 == nt) mma_commit_w(&ctrl.acc_full[x]);
-            na[x] = u + 1;
-            progressed = true;
-          }
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss_w(tb + C::S_COL + x * kKT, tile::res_lo(q_lo, x, C::DC, k), tile::res_lo(k_lo, 0, C::DC, k), i128,
+                     k > 0);
+          mma_commit_w(&ctrl.s_full[x]);
         }
-        if (ns < nt) {
-          const int t = ns;
-          bool ready = mbar_test_w(&ctrl.st_full[t % kNS], (t / kNS) & 1);
-          if (ready && t >= 2)
-            for (int x = 0; x < nblk; ++x) ready = ready && mbar_test_w(&ctrl.s_empty[x][t & 1], ((t - 2) >> 1) & 1);
-          if (ready) {
-            tc_fence_after();
-            const uint32_t klo = desc_lo(st_a + (t % kNS) * C::STAGE, 16);
-            for (int x = 0; x < nblk; ++x) {
-#pragma unroll
-              for (int k = 0; k < D / 16; ++k)
-                mma_ss_w(tb + C::S_COL + x * 64 + (t & 1) * 32, tile::res_lo(res_l, x, C::DC, k),
-                          tile::kmaj_lo(klo, C::CH, 0, k), i32, k > 0);
-              mma_commit_w(&ctrl.s_full[x][t & 1]);
-            }
-            ++ns;
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          idle_since = 0;
-        } else if ((++idle & 63u) == 0u) {
-          // Spin on the probes (a sleep here delays the next issue by far more
-          // than the tile period); every 64 empty polls lane 0 reads the clock
-          // and the abort flag, and the decision is broadcast so the warp stays
-          // converged.
-          const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
-          const int aborting = __shfl_sync(0xffffffffu, *wt.abort, 0);
-          if (idle_since == 0) {
-            idle_since = now;
-          } else if (aborting) {
-            ok = false;
-          } else if (now - idle_since > wt.limit) {
-            if ((tid & 31) == 0) {
-              *wt.abort = 1;
-              atomicOr(p.err, kErrTimeout);
-            }
-            ok = false;
-          }
-        }
+        if (ok) mma_commit_w(&ctrl.k_empty[sk]);
       }
-      mma_commit_w(&ctrl.drain);
-      mbar_wait_drain(&ctrl.drain, 0, kDrainNs);
+      mma_commit_w(&ctrl.drain_s);
+      mbar_wait_drain(&ctrl.drain_s, 0, kDrainNs);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------ O += P V MMAs
+    if (live) {
+      const uint32_t id = idesc_bf16(kM, D, false, true);
+      bool ok = true;
+      for (int t = 0; ok && t < nt; ++t) {
+        const int sv = t % C::NV;
+        const uint32_t v_mn = desc_lo(sm0 + C::V_OFF + sv * C::TILE, kChunk);
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.v_full[sv], (t / C::NV) & 1, wt));
+        for (int x = 0; ok && x < nblk; ++x) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.p_full[x], t & 1, wt));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kKT / 16; ++kk)
+            mma_ts_w(tb + x * D, tb + C::S_COL + x * kKT + kk * 8, tile::mnmaj(v_mn, 0, kk), id,
+                     (t > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_w(&ctrl.o_done[x]);
+        }
+        if (ok) mma_commit_w(&ctrl.v_empty[sv]);
+      }
+      mma_commit_w(&ctrl.drain_p);
+      mbar_wait_drain(&ctrl.drain_p, 0, kDrainNs);
     }
   } else {
     // ------------------------------------------------------------ softmax
     const int x = warp >> 2;                 // block owned by this warpgroup
     const int r = tid & 127;
     const uint32_t lane = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_col = tb + lane + C::S_COL + x * kKT;
     const float sc = p.tau * kLog2e;
     float m = -INFINITY, l = 0.f;
     bool ok = live && x < nblk;
     for (int t = 0; t < nt && ok; ++t) {
-      const int b = t & 1, k = t >> 1;
-      if (!mbar_wait(&ctrl.s_full[x][b], k & 1, wt)) { ok = false; break; }
+      if (!mbar_wait(&ctrl.s_full[x], t & 1, wt)) { ok = false; break; }
       tc_fence_after();
-      float s[32];
-      tmem_ld32(tb + lane + C::S_COL + x * 64 + b * 32, s);
-      tc_fence_before();
-      mbar_arrive(&ctrl.s_empty[x][b]);
+      // pass 1: tile row max
       float mt = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < kKT / 32; ++c) {
+        float s[32];
+        tmem_ld32(s_col + 32 * c, s);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        s[j] *= sc;
-        mt = fmaxf(mt, s[j]);
+        for (int j = 0; j < 32; ++j) mt = fmaxf(mt, s[j]);
       }
+      mt *= sc;
       if (__any_sync(0xffffffffu, mt > m + kRescale)) {
         const float mn = fmaxf(m, mt);
         if (t > 0) {
           const float scale = tile::ex2(m - mn);
           // the previous P V product of this block must have landed
-          if (!mbar_wait(&ctrl.o_empty[x][(t - 1) & 1], ((t - 1) >> 1) & 1, wt)) { ok = false; break; }
+          if (!mbar_wait(&ctrl.o_done[x], (t - 1) & 1, wt)) { ok = false; break; }
           tc_fence_after();
           const uint32_t ob = tb + lane + x * D;
 #pragma unroll 1
@@ -266,22 +245,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd2_tc(const __grid_constan
         }
         m = mn;
       }
-      uint32_t w[16];
+      // pass 2: P = 2^(x - m) as bf16 over the first 64 columns of S_X; chunk
+      // c writes columns 16c..16c+15, all already read (c/2 <= c)
       float ls = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < kKT / 32; ++c) {
+        float s[32];
+        tmem_ld32(s_col + 32 * c, s);
+        uint32_t w[16];
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        const float p0 = tile::ex2(s[j] - m), p1 = tile::ex2(s[j + 1] - m);
-        ls += p0 + p1;
-        w[j / 2] = pack_bf16x2(p0, p1);
+        for (int j = 0; j < 32; j += 2) {
+          const float p0 = tile::ex2(fmaf(s[j], sc, -m)), p1 = tile::ex2(fmaf(s[j + 1], sc, -m));
+          ls += p0 + p1;
+          w[j / 2] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16_nowait(s_col + 16 * c, w);
       }
       l += ls;
-      if (!mbar_wait(&ctrl.o_empty[x][b], (k & 1) ^ 1, wt)) { ok = false; break; }
-      tmem_st16_nowait(tb + lane + C::P_COL + x * 32 + b * 16, w);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&ctrl.o_full[x][b]);
+      mbar_arrive(&ctrl.p_full[x]);
     }
-    if (ok && mbar_wait(&ctrl.acc_full[x], 0, wt)) {
+    if (ok && mbar_wait(&ctrl.o_done[x], (nt - 1) & 1, wt)) {
       tc_fence_after();
       const int i = row0 + x * kM + r;
       const size_t ro = ((size_t)head * p.N + i) * D;
@@ -308,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd2_tc(const __grid_constan
 template <int D>
 cudaError_t fwd_d(const FwdArgs& a, const DevCtx& c, cudaStream_t s) {
   FwdParams p;
-  if (!make_bf16_map(&p.mQ, a.Q, a.BH, a.N, D, kM) || !make_bf16_map(&p.mK, a.K, a.BH, a.N, D, kT) ||
-      !make_bf16_map(&p.mV, a.V, a.BH, a.N, D, kT))
+  if (!make_bf16_map(&p.mQ, a.Q, a.BH, a.N, D, kM) || !make_bf16_map(&p.mK, a.K, a.BH, a.N, D, kKT) ||
+      !make_bf16_map(&p.mV, a.V, a.BH, a.N, D, kKT))
     return cudaErrorInvalidValue;
   p.O = a.O;
   p.L = a.L;
@@ -318,7 +303,7 @@ cudaError_t fwd_d(const FwdArgs& a, const DevCtx& c, cudaStream_t s) {
   p.err = c.err;
   p.wait_ns = c.wait_ns;
   p.stall = c.stall;
-  auto kernel = attn_fwd2_tc<D>;
+  auto kernel = attn_fwd_tc<D>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((a.N + 2 * kM - 1) / (2 * kM), a.BH);
