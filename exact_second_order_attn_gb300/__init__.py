@@ -10,3 +10,4 @@ from ._lib import (  # noqa: F401
     fbob_bob_workspace_bytes, fbob_debug_stall_producer, fbob_device_status, fbob_profile_enable,
     fbob_profile_report, fbob_set_wait_limit_ns, load, problem_for,
 )
+from .autograd import attention, hvp  # noqa: F401

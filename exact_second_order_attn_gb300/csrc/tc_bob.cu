@@ -97,6 +97,7 @@ __device__ __forceinline__ void load_tile2(const CUtensorMap* m0, const CUtensor
 template <int D_>
 struct PassU1 {
   using Params = P1Params;
+  static constexpr bool SPLIT = false;
   static constexpr int D = D_, DC = D / 64, T = 32;
   static constexpr bool kWide = D == 128;
   static constexpr int TRES = kWide ? 2 : 3;            // Q, UQ (, dO)
@@ -229,6 +230,7 @@ struct PassU1 {
 template <int D_>
 struct PassZ {
   using Params = P1Params;
+  static constexpr bool SPLIT = false;
   static constexpr int D = D_, DC = D / 64, T = 64, BLK = T * 128;
   static constexpr int RES = 0, TRES = 2;   // Q, dO
   static constexpr int ACH = BLK, BCH = BLK;
@@ -338,6 +340,7 @@ struct PassZ {
 template <int D_>
 struct PassY {
   using Params = P1Params;
+  static constexpr bool SPLIT = false;
   static constexpr int D = D_, DC = D / 64, T = D == 128 ? 32 : 64, BLK = T * 128;
   static constexpr int RES = 0, TRES = 2;   // Q, UQ
   static constexpr int ACH = 2 * BLK, BCH = 2 * BLK;
@@ -451,7 +454,7 @@ struct Pass2 {
   static constexpr int TRES = kAllTmem ? 4 : 2;    // K, UK (, V, UV)
   static constexpr int RES = kAllTmem ? 0 : 2 * DC * kChunk;   // V, UV in shared memory
   static constexpr int ACH = 3 * kBlk;            // [Q | UQ | dO] per chunk
-  static constexpr int VEC_OFF = DC * ACH;        // L (32), D (32), (alpha, E) (64) floats
+  static constexpr int VEC_OFF = DC * ACH;        // L (T), D (T), (alpha, E) (2T) floats
   static constexpr int SA = DC * ACH + 1024, SA_TX = DC * ACH + 512;
   static constexpr int SB = 0, SB_TX = 0;
   static constexpr int NSA = kAllTmem ? 8 : 4, NSB = 0;
@@ -533,33 +536,38 @@ struct Pass2 {
   struct Row {};
   __device__ static void ew_init(Row&, const Params&, int, int, int) {}
 
+  // Query columns per warpgroup and tile (all of them: the split of columns
+  // between the warpgroups measured slower here).
+  static constexpr bool SPLIT = false;
+  static constexpr int NC = SPLIT ? T / 2 : T;
   __device__ static bool ew_tile(Row&, const Params& p, const TileArgs& a, const TileSync& s, int r) {
     const float sc = p.tau * kLog2e;
-    const float* vL = a.vec;
-    const float* vD = a.vec + 32;
-    const float2* vAE = reinterpret_cast<const float2*>(a.vec + 64);
-    uint32_t wdS[16], wGs[16], wGd[16];
+    const float* vL = a.vec + a.c0;
+    const float* vD = a.vec + T + a.c0;
+    const float2* vAE = reinterpret_cast<const float2*>(a.vec + 2 * T) + a.c0;
+    uint32_t wdS[NC / 2], wGs[NC / 2], wGd[NC / 2];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < NC / 16; ++q) {
       float S[16], B[16], dP[16], C[16];
-      tmem_ld16x4(a.sc + q * 16, a.sc + 32 + q * 16, a.sc + 64 + q * 16, a.sc + 96 + q * 16, S, B, dP, C);
-      if (q == 1) s.release_scores();
+      const uint32_t c = a.sc + a.c0 + q * 16;
+      tmem_ld16x4(c, c + T, c + 2 * T, c + 3 * T, S, B, dP, C);
+      if (q == NC / 16 - 1) s.release_scores();
 #pragma unroll
-      for (int c = 0; c < 16; c += 2) {
+      for (int j = 0; j < 16; j += 2) {
         float dsv[2], gsv[2], gdv[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int ii = q * 16 + c + e;   // query column within the tile
+          const int ii = q * 16 + j + e;   // query column (relative to a.c0)
           const float Dq = vD[ii];
           const float2 ae = vAE[ii];
-          const float pe = ex2(fmaf(S[c + e], sc, -vL[ii] * kLog2e));
-          const float te = dP[c + e] - Dq;
-          const float bp = fmaf(p.tau, B[c + e], -ae.x);
+          const float pe = ex2(fmaf(S[j + e], sc, -vL[ii] * kLog2e));
+          const float te = dP[j + e] - Dq;
+          const float bp = fmaf(p.tau, B[j + e], -ae.x);
           dsv[e] = pe * te;
-          gsv[e] = pe * (fmaf(bp, te, C[c + e]) + fmaf(ae.x, Dq, -ae.y));
+          gsv[e] = pe * (fmaf(bp, te, C[j + e]) + fmaf(ae.x, Dq, -ae.y));
           gdv[e] = pe * bp;
         }
-        const int k = q * 8 + c / 2;
+        const int k = q * 8 + j / 2;
         wdS[k] = pack_bf16x2(dsv[0], dsv[1]);
         wGs[k] = pack_bf16x2(gsv[0], gsv[1]);
         wGd[k] = pack_bf16x2(gdv[0], gdv[1]);
@@ -567,13 +575,18 @@ struct Pass2 {
     }
     if (!s.acquire_ops()) return false;
     if (kAllTmem) {
-      tmem_st16_nowait(a.ops, wdS);
-      tmem_st16_nowait(a.ops + 16, wGs);
-      tmem_st16_nowait(a.ops + 32, wGd);
+      const uint32_t o = a.ops + a.c0 / 2;
+#pragma unroll
+      for (int c = 0; c < NC / 16; ++c) {
+        tmem_st8_nowait(o + 8 * c, wdS + 8 * c);
+        tmem_st8_nowait(o + 16 + 8 * c, wGs + 8 * c);
+        tmem_st8_nowait(o + 32 + 8 * c, wGd + 8 * c);
+      }
     } else {
-      write_op_half(a.ops, r, a.h, wdS);
-      write_op_half(a.ops + kChunk, r, a.h, wGs);
-      write_op_half(a.ops + 2 * kChunk, r, a.h, wGd);
+      const int col = 32 * (int)a.h + a.c0;
+      write_op_cols<NC / 2>(a.ops, (uint32_t)r, col, wdS);
+      write_op_cols<NC / 2>(a.ops + kChunk, (uint32_t)r, col, wGs);
+      write_op_cols<NC / 2>(a.ops + 2 * kChunk, (uint32_t)r, col, wGd);
     }
     s.publish_ops();
     return true;

@@ -47,6 +47,7 @@ struct DqParams {
 template <int D_>
 struct DqOp {
   using Params = DqParams;
+  static constexpr bool SPLIT = false;
   static constexpr int D = D_, DC = D / 64, T = 64, BLK = T * 128;
   static constexpr int RES = 0, TRES = 2;
   static constexpr int ACH = BLK, BCH = BLK;
@@ -222,16 +223,20 @@ struct DkvOp {
   }
   struct Row {};
   __device__ static void ew_init(Row&, const Params&, int, int, int) {}
+  // NC query columns per warpgroup and tile: all T with two score buffers,
+  // T / 2 (starting at a.c0) when both warpgroups share the one buffer.
+  static constexpr bool SPLIT = NBUF == 1;
+  static constexpr int NC = SPLIT ? T / 2 : T;
   __device__ static bool ew_tile(Row&, const Params& p, const tile::TileArgs& a, const tile::TileSync& s, int r) {
     const float sc = p.tau * tile::kLog2e;
-    const float* vL = a.vec;
-    const float* vD = a.vec + T;
-    uint32_t wP[T / 2], wd[T / 2];
+    const float* vL = a.vec + a.c0;
+    const float* vD = a.vec + T + a.c0;
+    uint32_t wP[NC / 2], wd[NC / 2];
 #pragma unroll
-    for (int q = 0; q < T / 16; ++q) {
+    for (int q = 0; q < NC / 16; ++q) {
       float S[16], dP[16];
-      tmem_ld16x2(a.sc + q * 16, a.sc + T + q * 16, S, dP);
-      if (q == T / 16 - 1) s.release_scores();
+      tmem_ld16x2(a.sc + a.c0 + q * 16, a.sc + T + a.c0 + q * 16, S, dP);
+      if (q == NC / 16 - 1) s.release_scores();
 #pragma unroll
       for (int c = 0; c < 16; c += 2) {
         const int ii = q * 16 + c;
@@ -242,8 +247,8 @@ struct DkvOp {
       }
     }
     if (!s.acquire_ops()) return false;
-    tile::write_op64(a.ops + a.h * tile::kChunk, (uint32_t)r, wP);
-    tile::write_op64(a.ops + (2 + a.h) * tile::kChunk, (uint32_t)r, wd);
+    tile::write_op_cols<NC / 2>(a.ops + a.h * tile::kChunk, (uint32_t)r, a.c0, wP);
+    tile::write_op_cols<NC / 2>(a.ops + (2 + a.h) * tile::kChunk, (uint32_t)r, a.c0, wd);
     s.publish_ops();
     return true;
   }

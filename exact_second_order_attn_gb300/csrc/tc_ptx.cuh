@@ -281,6 +281,11 @@ __device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t*
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st8_nowait(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
 
 // Store 8 consecutive 32-bit columns of this thread's lane and wait.
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {

@@ -5,9 +5,12 @@
 //
 // CTA of 11 warps:
 //   warps 0-7  two elementwise warpgroups; warpgroup g handles the streamed
-//              tiles t with t % 2 == g, so one group works on tile t while the
-//              other works on tile t+1.  Thread r of either group owns TMEM
-//              lane r = tile row r (row sums are thread-local).
+//              tiles t with t % 2 == g, so one group works on tile t while
+//              the other works on tile t+1 - or, for a policy with one score
+//              buffer that asks for it (SPLIT), both work on every tile, group
+//              g on its half of the tile's columns, so the buffer is read and
+//              released in half the time.  Thread r of either group owns TMEM
+//              lane r = resident row r (row sums are thread-local partials).
 //   warp 8     TMA producer (one thread).
 //   warp 9     issues the score MMAs; TMEM owner (512 columns).
 //   warp 10    issues the accumulator MMAs.
@@ -109,18 +112,22 @@ struct Ctrl {
 struct TileSync {
   Ctrl* c;
   const Waiter* w;
-  int q;          // tile parity = warpgroup
-  int k;          // tile index within this warpgroup
+  int q;          // tile parity: score/operand barrier and operand half
+  int k;          // t >> 1
   int sa;         // ring-A stage of the tile
   bool vec;       // the tile's ring-A stage carries vectors read by the warpgroup
   bool ts;        // operands go to TMEM
 #ifdef FBOB_TRACE
-  bool trace_on;
+  bool trace_on, trace_all;
   int t;
 #endif
 
   // scores of this tile are in registers: the TMEM buffer may be reused
   __device__ __forceinline__ void release_scores() const {
+    FBOB_STAMP(3, t);
+#ifdef FBOB_TRACE
+    if (trace_all && t < 64) g_trace[(11 + ((threadIdx.x >> 5) & 7) / 2) * 64 + t] = clock64();  // warps 1,3,5,7 -> 11..14
+#endif
     tc_fence_before();
     mbar_arrive(&c->s_empty[q]);
   }
@@ -176,12 +183,16 @@ struct TileArgs {
   uint32_t ops;        // SS: shared address of operand tile 0; TS: TMEM address of the half's first column
   uint32_t h;          // operand half (SS: columns 32h..32h+31 of each [128][64] operand tile)
   int t;               // tile index
+  int c0;              // first tile column this warpgroup handles (0, or T/2 when the columns are split)
 };
 
 template <class Op>
 __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant__ typename Op::Params p) {
   static_assert(Op::NSB == 0 || Op::NSB == Op::NSA, "ring B stages pair with ring A stages");
   static_assert(Op::NBUF < Op::NSA, "the MMA order needs more stages than score buffers");
+  constexpr bool kSplit = Op::SPLIT;  // both warpgroups on every tile, half the columns each
+  static_assert(!kSplit || Op::NBUF == 1, "split columns only with one score buffer");
+  constexpr int kEwPerTile = kSplit ? 256 : 128;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ Ctrl ctrl;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -198,13 +209,13 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
     mbar_init(&ctrl.tres_full, 256);
     for (int s = 0; s < Op::NSA; ++s) {
       mbar_init(&ctrl.a_full[s], 1);
-      mbar_init(&ctrl.a_empty[s], Op::VEC ? 1 + 4 : 1);
+      mbar_init(&ctrl.a_empty[s], Op::VEC ? 1 + kEwPerTile / 32 : 1);
     }
     for (int s = 0; s < Op::NSB; ++s) mbar_init(&ctrl.b_empty[s], 1);
     for (int q = 0; q < 2; ++q) {
       mbar_init(&ctrl.s_full[q], 1);
-      mbar_init(&ctrl.s_empty[q], 128);
-      mbar_init(&ctrl.o_full[q], 128);
+      mbar_init(&ctrl.s_empty[q], kEwPerTile);
+      mbar_init(&ctrl.o_full[q], kEwPerTile);
       mbar_init(&ctrl.o_empty[q], 1);
     }
     mbar_init(&ctrl.acc_full, 1);
@@ -287,12 +298,18 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
         const int sa = t % Op::NSA, u = t - Op::NBUF;
         // both conditions probed in one go (their latencies overlap); the
         // bounded blocking waits only run when a probe found one incomplete
+        FBOB_STAMP(4, t);
+        // both conditions probed in one go (their latencies overlap); the
+        // bounded blocking waits only run when the probe found one incomplete
         uint64_t* eb = &ctrl.s_empty[(u < 0 ? 0 : u) & 1];
-        const uint32_t ep = u < 0 ? 1u : (uint32_t)((u >> 1) & 1);   // parity 1 of a fresh barrier: complete
-        if (!__all_sync(0xffffffffu, mbar_test2(&ctrl.a_full[sa], (t / Op::NSA) & 1, eb, ep)))
-          ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.a_full[sa], (t / Op::NSA) & 1, wt) &&
-                                           (u < 0 || mbar_wait(&ctrl.s_empty[u & 1], (u >> 1) & 1, wt)));
+        const uint32_t ep = u < 0 ? 1u : (uint32_t)((u >> 1) & 1);
+        if (u < 0 || !__all_sync(0xffffffffu, mbar_test2(&ctrl.a_full[sa], (t / Op::NSA) & 1, eb, ep))) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.a_full[sa], (t / Op::NSA) & 1, wt));
+          FBOB_STAMP(15, t);
+          ok = ok && __all_sync(0xffffffffu, u < 0 || mbar_wait(&ctrl.s_empty[u & 1], (u >> 1) & 1, wt));
+        }
         if (!ok) break;
+        FBOB_STAMP(5, t);
         tc_fence_after();
         FBOB_STAMP(9, t);
         Op::score_mmas(tb + Op::ACC + (t % Op::NBUF) * Op::SCOLS, tres, res_l, desc_lo(ra + sa * Op::SA, 16),
@@ -356,29 +373,28 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
     }
     Op::ew_init(row, p, blk0, r, head);
     bool ok = live;
-    for (int t = g; t < nt && ok; t += 2) {
-      const int k = t >> 1, sa = t % Op::NSA;
+    for (int t = kSplit ? 0 : g; t < nt && ok; t += kSplit ? 1 : 2) {
+      const int q = t & 1, k = t >> 1, sa = t % Op::NSA;
       FBOB_STAMP(8, t);
       if (Op::VEC && !mbar_wait(&ctrl.a_full[sa], (t / Op::NSA) & 1, wt)) { ok = false; break; }
-      if (!mbar_wait(&ctrl.s_full[g], k & 1, wt)) { ok = false; break; }
+      if (!mbar_wait(&ctrl.s_full[q], k & 1, wt)) { ok = false; break; }
       FBOB_STAMP(2, t);
       tc_fence_after();
 #ifdef FBOB_TRACE
-      const TileSync sync{&ctrl, &wt, g, k, sa, Op::VEC, Op::TS, trace_on, t};
+      const TileSync sync{&ctrl, &wt, q, k, sa, Op::VEC, Op::TS, trace_on, trace_cta && ((warp & 1) == 1), t};
 #else
-      const TileSync sync{&ctrl, &wt, g, k, sa, Op::VEC, Op::TS};
+      const TileSync sync{&ctrl, &wt, q, k, sa, Op::VEC, Op::TS};
 #endif
       TileArgs ta;
       ta.sc = tb + lane + Op::ACC + (t % Op::NBUF) * Op::SCOLS;
       ta.vec = Op::VEC ? reinterpret_cast<const float*>(ring_a + sa * Op::SA + Op::VEC_OFF) : nullptr;
-      ta.ops = Op::TS ? (tb + lane + Op::OP_COL + (uint32_t)g * Op::OP_HALF) : smem_u32(ops);
-      ta.h = (uint32_t)g;
+      ta.ops = Op::TS ? (tb + lane + Op::OP_COL + (uint32_t)q * Op::OP_HALF) : smem_u32(ops);
+      ta.h = (uint32_t)q;
       ta.t = t;
+      ta.c0 = kSplit ? g * (Op::T / 2) : 0;
       ok = Op::ew_tile(row, p, ta, sync, r);
       FBOB_STAMP(6, t);
-#ifdef FBOB_TRACE
-      if (trace_cta && t < 64) g_trace[(11 + (warp & 3)) * 64 + t] = clock64();
-#endif
+
     }
     const EpiArgs ea{tb + lane, reinterpret_cast<float*>(ring_a), &ctrl, &wt, blk0, r, head, g};
     if (ok && mbar_wait(&ctrl.acc_full, 0, wt)) {
@@ -444,6 +460,16 @@ __device__ __forceinline__ void write_op64(uint32_t tile, uint32_t r, const uint
 #pragma unroll
   for (int cc = 0; cc < 8; ++cc)
     st_shared_v4(tile + sw128_offset(r, cc), w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
+}
+
+// Write NW packed words (2 NW bf16) of row r into columns [col0, col0 + 2 NW)
+// of a 128B-swizzled [128][64] operand tile (col0 a multiple of 8).
+template <int NW>
+__device__ __forceinline__ void write_op_cols(uint32_t tile, uint32_t r, int col0, const uint32_t* w) {
+#pragma unroll
+  for (int cc = 0; cc < NW / 4; ++cc)
+    st_shared_v4(tile + sw128_offset(r, (uint32_t)(col0 / 8 + cc)), w[4 * cc], w[4 * cc + 1], w[4 * cc + 2],
+                 w[4 * cc + 3]);
 }
 
 // Write 32 packed bf16 (16 words) of row r into columns [32h, 32h+32) of a
