@@ -38,7 +38,11 @@ Readings where the pages are silent (each is also listed in the design doc):
   D = rowsum(dO o O) is differentiated through O = P V.
 * tau multiplies the scores once: S = tau Q K^T.
 * L is the natural-log row logsumexp.
-* Non-causal attention.
+* Non-causal attention by default.  The pages never state a mask; with
+  ``causal=True`` the plain definition of causal attention is used: query i
+  attends to keys j <= i (S_ij = -inf for j > i before the row softmax).
+  Every reverse-mode step below multiplies by P, so the masked entries drop
+  out of all derivatives without further changes.
 
 Every row of every intermediate (S, P, O, dP, D, dS) depends only on the
 query rows of Q and dO of that row, so the graph of g splits exactly into
@@ -78,6 +82,16 @@ def _f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
+def _mask(S: np.ndarray, qidx) -> np.ndarray:
+    """Causal mask: S_aj = -inf where key j comes after query qidx[a]
+    (qidx None: no mask).  Key 0 is never masked, so every row keeps a
+    finite maximum."""
+    if qidx is None:
+        return S
+    keys = np.arange(S.shape[1])
+    return np.where(keys[None, :] > np.asarray(qidx)[:, None], -np.inf, S)
+
+
 def _softmax_rows(S: np.ndarray):
     """Row softmax and natural-log logsumexp with the usual max shift."""
     m = S.max(axis=1, keepdims=True)
@@ -92,10 +106,11 @@ def _softmax_rows(S: np.ndarray):
 # forward (abstract: FlashAttention-style forward; here materialised)
 # ---------------------------------------------------------------------------
 
-def attn_fwd_head(Q, K, V, tau):
-    """O = softmax(tau Q K^T) V and L = logsumexp rows, one head, fp64."""
+def attn_fwd_head(Q, K, V, tau, qidx=None):
+    """O = softmax(tau Q K^T) V and L = logsumexp rows, one head, fp64
+    (rows of Q are the queries qidx under the causal mask, if given)."""
     Q, K, V = _f64(Q), _f64(K), _f64(V)
-    S = tau * (Q @ K.T)
+    S = _mask(tau * (Q @ K.T), qidx)
     P, L = _softmax_rows(S)
     O = P @ V
     return O, L
@@ -105,14 +120,15 @@ def attn_fwd_head(Q, K, V, tau):
 # first backward g (abstract; evolve.pub FAQ "What is backward-over-backward")
 # ---------------------------------------------------------------------------
 
-def attn_bwd_rows(Qr, K, V, dOr, tau):
-    """First backward restricted to the query rows Qr, dOr of one head.
+def attn_bwd_rows(Qr, K, V, dOr, tau, qidx=None):
+    """First backward restricted to the query rows Qr, dOr of one head
+    (query indices qidx under the causal mask, if given).
 
     Returns (dQ_rows, dK_part, dV_part, D_rows): the row outputs are complete,
     the key-side outputs are this block's contribution to the sums over rows.
     """
     Qr, K, V, dOr = _f64(Qr), _f64(K), _f64(V), _f64(dOr)
-    S = tau * (Qr @ K.T)
+    S = _mask(tau * (Qr @ K.T), qidx)
     P, _ = _softmax_rows(S)
     O = P @ V
     dV = P.T @ dOr
@@ -130,9 +146,9 @@ def attn_bwd_rows(Qr, K, V, dOr, tau):
 # Appendix C)
 # ---------------------------------------------------------------------------
 
-def bob_rows(Qr, K, V, dOr, UQr, UK, UV, tau):
+def bob_rows(Qr, K, V, dOr, UQr, UK, UV, tau, qidx=None):
     """Reverse-mode sweep of f = <UQ,dQ> + <UK,dK> + <UV,dV> for one query-row
-    block of one head.
+    block of one head (query indices qidx under the causal mask, if given).
 
     Returns (gQ_rows, gK_part, gV_part, gdO_rows).  Every node of the first
     backward is materialised; adjoints are named ``<node>_bar``.
@@ -141,7 +157,7 @@ def bob_rows(Qr, K, V, dOr, UQr, UK, UV, tau):
     UQr, UK, UV = _f64(UQr), _f64(UK), _f64(UV)
 
     # ---- forward sweep: the nodes of g ---------------------------------
-    S = tau * (Qr @ K.T)                      # S = tau Q K^T
+    S = _mask(tau * (Qr @ K.T), qidx)         # S = tau Q K^T (masked)
     P, _ = _softmax_rows(S)                   # P = softmax_row(S)
     O = P @ V                                 # O = P V
     dP = dOr @ V.T                            # dP = dO V^T
@@ -188,7 +204,7 @@ def bob_rows(Qr, K, V, dOr, UQr, UK, UV, tau):
     return Q_bar, K_bar, V_bar, dO_bar
 
 
-def row_scalars(Qr, K, V, dOr, UQr, UK, UV, tau):
+def row_scalars(Qr, K, V, dOr, UQr, UK, UV, tau, qidx=None):
     """The two row scalars of the hierarchical affine structure for a row block.
 
     The pages name them alpha and E (evolve.pub review, Summary and Key claims:
@@ -204,7 +220,7 @@ def row_scalars(Qr, K, V, dOr, UQr, UK, UV, tau):
     """
     Qr, K, V, dOr = _f64(Qr), _f64(K), _f64(V), _f64(dOr)
     UQr, UK, UV = _f64(UQr), _f64(UK), _f64(UV)
-    S = tau * (Qr @ K.T)
+    S = _mask(tau * (Qr @ K.T), qidx)
     P, _ = _softmax_rows(S)
     dP = dOr @ V.T
     B = tau * (UQr @ K.T + Qr @ UK.T)
@@ -230,7 +246,11 @@ def _heads(x):
     return x.reshape((-1,) + x.shape[-2:]), lead
 
 
-def attn_fwd(Q, K, V, tau):
+def _qidx(rows, causal):
+    return np.arange(rows.start, rows.stop) if causal else None
+
+
+def attn_fwd(Q, K, V, tau, causal=False):
     """O [..., N, d], L [..., N] for every head of [..., N, d] inputs."""
     Qh, lead = _heads(Q)
     Kh, _ = _heads(K)
@@ -239,11 +259,11 @@ def attn_fwd(Q, K, V, tau):
     L = np.empty(Qh.shape[:-1])
     for h in range(Qh.shape[0]):
         for rows in _row_blocks(Qh.shape[1]):
-            O[h, rows], L[h, rows] = attn_fwd_head(Qh[h, rows], Kh[h], Vh[h], tau)
+            O[h, rows], L[h, rows] = attn_fwd_head(Qh[h, rows], Kh[h], Vh[h], tau, _qidx(rows, causal))
     return O.reshape(lead + O.shape[1:]), L.reshape(lead + L.shape[1:])
 
 
-def attn_bwd(Q, K, V, dO, tau):
+def attn_bwd(Q, K, V, dO, tau, causal=False):
     """(dQ, dK, dV, D) for every head of [..., N, d] inputs."""
     Qh, lead = _heads(Q)
     Kh, _ = _heads(K)
@@ -255,7 +275,7 @@ def attn_bwd(Q, K, V, dO, tau):
     D = np.empty(Qh.shape[:-1])
     for h in range(Qh.shape[0]):
         for rows in _row_blocks(Qh.shape[1]):
-            q, k, v, dd = attn_bwd_rows(Qh[h, rows], Kh[h], Vh[h], dOh[h, rows], tau)
+            q, k, v, dd = attn_bwd_rows(Qh[h, rows], Kh[h], Vh[h], dOh[h, rows], tau, _qidx(rows, causal))
             dQ[h, rows] = q
             dK[h] += k
             dV[h] += v
@@ -264,7 +284,7 @@ def attn_bwd(Q, K, V, dO, tau):
     return shp(dQ), shp(dK), shp(dV), shp(D)
 
 
-def attn_bob(Q, K, V, dO, UQ, UK, UV, tau):
+def attn_bob(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
     """(gQ, gK, gV, gdO) for every head of [..., N, d] inputs."""
     Qh, lead = _heads(Q)
     Kh, _ = _heads(K)
@@ -280,7 +300,7 @@ def attn_bob(Q, K, V, dO, UQ, UK, UV, tau):
     for h in range(Qh.shape[0]):
         for rows in _row_blocks(Qh.shape[1]):
             q, k, v, o = bob_rows(Qh[h, rows], Kh[h], Vh[h], dOh[h, rows],
-                                  UQh[h, rows], UKh[h], UVh[h], tau)
+                                  UQh[h, rows], UKh[h], UVh[h], tau, _qidx(rows, causal))
             gQ[h, rows] = q
             gK[h] += k
             gV[h] += v
@@ -289,7 +309,7 @@ def attn_bob(Q, K, V, dO, UQ, UK, UV, tau):
     return shp(gQ), shp(gK), shp(gV), shp(gdO)
 
 
-def bob_row_scalars(Q, K, V, dO, UQ, UK, UV, tau):
+def bob_row_scalars(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
     """(alpha, E) [..., N] for every head (see ``row_scalars``)."""
     Qh, lead = _heads(Q)
     Kh, _ = _heads(K)
@@ -303,16 +323,17 @@ def bob_row_scalars(Q, K, V, dO, UQ, UK, UV, tau):
     for h in range(Qh.shape[0]):
         for rows in _row_blocks(Qh.shape[1]):
             alpha[h, rows], E[h, rows] = row_scalars(
-                Qh[h, rows], Kh[h], Vh[h], dOh[h, rows], UQh[h, rows], UKh[h], UVh[h], tau)
+                Qh[h, rows], Kh[h], Vh[h], dOh[h, rows], UQh[h, rows], UKh[h], UVh[h], tau, _qidx(rows, causal))
     return alpha.reshape(lead + alpha.shape[1:]), E.reshape(lead + E.shape[1:])
 
 
-def bob_sampled_rows(Q, K, V, dO, UQ, UK, UV, tau, rows):
+def bob_sampled_rows(Q, K, V, dO, UQ, UK, UV, tau, rows, causal=False):
     """Query-row outputs (gQ, gdO) of one head restricted to the given rows.
 
     The row-side outputs of a row are complete from that row alone (see the
     module docstring), so long sequences can be checked on a sample of rows.
     """
     rows = np.asarray(rows)
-    gQ, _, _, gdO = bob_rows(_f64(Q)[rows], K, V, _f64(dO)[rows], _f64(UQ)[rows], UK, UV, tau)
+    gQ, _, _, gdO = bob_rows(_f64(Q)[rows], K, V, _f64(dO)[rows], _f64(UQ)[rows], UK, UV, tau,
+                             rows if causal else None)
     return gQ, gdO
