@@ -135,9 +135,10 @@ def _empty(ref, shape=None):
     return torch.empty(ref.shape if shape is None else shape, dtype=torch.float32, device=ref.device)
 
 
-def fbob_attn_fwd(Q, K, V, tau, O=None, L=None, stream=None):
-    """(O, L) = forward; allocates O, L if not given."""
-    p = problem_for(Q, tau)
+def fbob_attn_fwd(Q, K, V, tau, O=None, L=None, stream=None, causal=False):
+    """(O, L) = forward; allocates O, L if not given.  ``causal``: query i
+    attends to keys j <= i."""
+    p = problem_for(Q, tau, causal)
     O = _empty(Q) if O is None else O
     L = _empty(Q, Q.shape[:3]) if L is None else L
     _same(Q, K, V, dtype=Q.dtype, shape=Q.shape)
@@ -147,9 +148,9 @@ def fbob_attn_fwd(Q, K, V, tau, O=None, L=None, stream=None):
     return O, L
 
 
-def fbob_attn_bwd(Q, K, V, O, dO, L, tau, dQ=None, dK=None, dV=None, D=None, stream=None):
+def fbob_attn_bwd(Q, K, V, O, dO, L, tau, dQ=None, dK=None, dV=None, D=None, stream=None, causal=False):
     """(dQ, dK, dV, D) = first backward; allocates outputs if not given."""
-    p = problem_for(Q, tau)
+    p = problem_for(Q, tau, causal)
     dQ = _empty(Q) if dQ is None else dQ
     dK = _empty(Q) if dK is None else dK
     dV = _empty(Q) if dV is None else dV
@@ -168,12 +169,12 @@ def fbob_bob_workspace_bytes(Q):
 
 
 def fbob_attn_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ=None, gK=None, gV=None, gdO=None,
-                  workspace=None, stream=None):
+                  workspace=None, stream=None, causal=False):
     """(gQ, gK, gV, gdO, workspace) = BoB; allocates outputs/workspace if not given.
 
     ``workspace`` is a float32 tensor [B, H, N, 2] holding (alpha, E) per row.
     """
-    p = problem_for(Q, tau)
+    p = problem_for(Q, tau, causal)
     gQ = _empty(Q) if gQ is None else gQ
     gK = _empty(Q) if gK is None else gK
     gV = _empty(Q) if gV is None else gV
@@ -192,9 +193,9 @@ def fbob_attn_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ=None, gK=None, gV=No
 
 
 def fbob_attn_bob_noalloc(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ=None, gK=None, gV=None, gdO=None,
-                          stream=None):
+                          stream=None, causal=False):
     """(gQ, gK, gV, gdO) = BoB with the library's fixed workspace (no workspace argument)."""
-    p = problem_for(Q, tau)
+    p = problem_for(Q, tau, causal)
     gQ = _empty(Q) if gQ is None else gQ
     gK = _empty(Q) if gK is None else gK
     gV = _empty(Q) if gV is None else gV

@@ -44,43 +44,45 @@ class _AttnBwd(torch.autograd.Function):
     """(Q, K, V, dO) -> (dQ, dK, dV); its own backward is BoB."""
 
     @staticmethod
-    def forward(ctx, Q, K, V, dO, O, L, tau):
-        dQ, dK, dV, D = _lib.fbob_attn_bwd(Q, K, V, O, dO, L, tau)
+    def forward(ctx, Q, K, V, dO, O, L, tau, causal):
+        dQ, dK, dV, D = _lib.fbob_attn_bwd(Q, K, V, O, dO, L, tau, causal=causal)
         ctx.save_for_backward(Q, K, V, dO, O, L, D)
-        ctx.tau = tau
+        ctx.tau, ctx.causal = tau, causal
         return dQ, dK, dV
 
     @staticmethod
     @once_differentiable
     def backward(ctx, UQ, UK, UV):
         Q, K, V, dO, O, L, D = ctx.saved_tensors
-        gQ, gK, gV, gdO, _ = _lib.fbob_attn_bob(Q, K, V, O, dO, L, D, _as(UQ, Q), _as(UK, Q), _as(UV, Q), ctx.tau)
-        return gQ.to(Q.dtype), gK.to(K.dtype), gV.to(V.dtype), gdO.to(dO.dtype), None, None, None
+        gQ, gK, gV, gdO, _ = _lib.fbob_attn_bob(Q, K, V, O, dO, L, D, _as(UQ, Q), _as(UK, Q), _as(UV, Q), ctx.tau,
+                                                causal=ctx.causal)
+        return gQ.to(Q.dtype), gK.to(K.dtype), gV.to(V.dtype), gdO.to(dO.dtype), None, None, None, None
 
 
 class _Attn(torch.autograd.Function):
     """(Q, K, V) -> O; its backward is the differentiable _AttnBwd."""
 
     @staticmethod
-    def forward(ctx, Q, K, V, tau):
-        O, L = _lib.fbob_attn_fwd(Q, K, V, tau)
+    def forward(ctx, Q, K, V, tau, causal):
+        O, L = _lib.fbob_attn_fwd(Q, K, V, tau, causal=causal)
         ctx.save_for_backward(Q, K, V, O, L)
-        ctx.tau = tau
+        ctx.tau, ctx.causal = tau, causal
         return O
 
     @staticmethod
     def backward(ctx, gO):
         Q, K, V, O, L = ctx.saved_tensors
         dO = _as(gO, Q)
-        dQ, dK, dV = _AttnBwd.apply(Q, K, V, dO, O.detach(), L.detach(), ctx.tau)
-        return dQ.to(Q.dtype), dK.to(K.dtype), dV.to(V.dtype), None
+        dQ, dK, dV = _AttnBwd.apply(Q, K, V, dO, O.detach(), L.detach(), ctx.tau, ctx.causal)
+        return dQ.to(Q.dtype), dK.to(K.dtype), dV.to(V.dtype), None, None
 
 
-def attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, tau: float) -> torch.Tensor:
-    """O = softmax(tau Q K^T) V for [B, H, N, d] tensors, twice differentiable."""
+def attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, tau: float, causal: bool = False) -> torch.Tensor:
+    """O = softmax(tau Q K^T) V for [B, H, N, d] tensors, twice differentiable
+    (``causal``: query i attends to keys j <= i)."""
     if not (Q.is_contiguous() and K.is_contiguous() and V.is_contiguous()):
         raise ValueError("Q, K, V must be contiguous")
-    return _Attn.apply(Q, K, V, float(tau))
+    return _Attn.apply(Q, K, V, float(tau), bool(causal))
 
 
 def hvp(loss_fn, params, vectors):

@@ -44,7 +44,6 @@ fbob_status check_problem(const fbob_problem* p, bool* empty) {
   if (p->dtype != FBOB_BF16 && p->dtype != FBOB_FP32)
     return fail(FBOB_ERR_INVALID_ARG, "unknown dtype %d", p->dtype);
   if (p->d != 64 && p->d != 128) return fail(FBOB_ERR_UNSUPPORTED, "head size d=%d (supported: 64, 128)", p->d);
-  if (p->causal != 0) return fail(FBOB_ERR_UNSUPPORTED, "causal masking is not supported");
   const long long heads = (long long)p->B * p->H;
   if (heads > 65535) return fail(FBOB_ERR_UNSUPPORTED, "B*H=%lld exceeds 65535", heads);
   if ((long long)p->N * p->d * heads > (1ll << 40))
@@ -118,7 +117,7 @@ fbob_status fbob_attn_fwd(const fbob_problem* p, const void* Q, const void* K, c
   if ((st = check_ptrs(ps, 5)) != FBOB_OK) return st;
   fbob::DevCtx c;
   if ((st = make_ctx(&c)) != FBOB_OK) return st;
-  fbob::FwdArgs a{Q, K, V, O, L, p->B * p->H, p->N, p->d, p->tau};
+  fbob::FwdArgs a{Q, K, V, O, L, p->B * p->H, p->N, p->d, p->tau, p->causal != 0};
   cudaError_t e = p->dtype == FBOB_BF16 ? fbob::tc_fwd(a, c, stream) : fbob::simt_fwd(a, c, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
   return FBOB_OK;
@@ -136,7 +135,7 @@ fbob_status fbob_attn_bwd(const fbob_problem* p, const void* Q, const void* K, c
   if ((st = check_ptrs(ps, 10)) != FBOB_OK) return st;
   fbob::DevCtx c;
   if ((st = make_ctx(&c)) != FBOB_OK) return st;
-  fbob::BwdArgs a{Q, K, V, dO, O, L, dQ, dK, dV, D, p->B * p->H, p->N, p->d, p->tau};
+  fbob::BwdArgs a{Q, K, V, dO, O, L, dQ, dK, dV, D, p->B * p->H, p->N, p->d, p->tau, p->causal != 0};
   cudaError_t e = p->dtype == FBOB_BF16 ? fbob::tc_bwd(a, c, stream) : fbob::simt_bwd(a, c, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
   return FBOB_OK;
@@ -160,7 +159,8 @@ fbob_status fbob_attn_bob(const fbob_problem* p, const void* Q, const void* K, c
     return fail(FBOB_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
   fbob::DevCtx c;
   if ((st = make_ctx(&c)) != FBOB_OK) return st;
-  fbob::BobArgs a{Q, K, V, dO, UQ, UK, UV, O, L, D, gQ, gK, gV, gdO, workspace, p->B * p->H, p->N, p->d, p->tau};
+  fbob::BobArgs a{Q, K, V, dO, UQ, UK, UV, O, L, D, gQ, gK, gV, gdO, workspace, p->B * p->H, p->N, p->d, p->tau,
+                  p->causal != 0};
   cudaError_t e = p->dtype == FBOB_BF16 ? fbob::tc_bob(a, c, stream) : fbob::simt_bob(a, c, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attn_bob launch");
   return FBOB_OK;
@@ -188,7 +188,8 @@ fbob_status fbob_attn_bob_noalloc(const fbob_problem* p, const void* Q, const vo
   if (e != cudaSuccess) return cuda_fail(e, "fixed workspace address");
   fbob::DevCtx c;
   if ((st = make_ctx(&c)) != FBOB_OK) return st;
-  fbob::BobArgs a{Q, K, V, dO, UQ, UK, UV, O, L, D, gQ, gK, gV, gdO, ws, p->B * p->H, p->N, p->d, p->tau};
+  fbob::BobArgs a{Q, K, V, dO, UQ, UK, UV, O, L, D, gQ, gK, gV, gdO, ws, p->B * p->H, p->N, p->d, p->tau,
+                  p->causal != 0};
   e = p->dtype == FBOB_BF16 ? fbob::tc_bob(a, c, stream) : fbob::simt_bob(a, c, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attn_bob_noalloc launch");
   return FBOB_OK;

@@ -21,6 +21,7 @@ struct FwdArgs {
   float *O, *L;
   int BH, N, d;
   float tau;
+  int causal;  // query i attends to keys j <= i
 };
 
 struct BwdArgs {
@@ -29,6 +30,7 @@ struct BwdArgs {
   float *dQ, *dK, *dV, *D;
   int BH, N, d;
   float tau;
+  int causal;
 };
 
 struct BobArgs {
@@ -38,6 +40,7 @@ struct BobArgs {
   float* ws;  // [BH, N, 2]: alpha, E
   int BH, N, d;
   float tau;
+  int causal;
 };
 
 // Status word bits.

@@ -26,6 +26,7 @@ namespace {
 
 constexpr int BR = 32;   // resident rows per CTA
 constexpr int BC = 32;   // streamed rows per tile
+static_assert(BR == BC, "the causal column loops start at the block's first row");
 constexpr int NT = 256;  // threads per CTA
 constexpr int LO = BC + 1;
 
@@ -79,7 +80,8 @@ __global__ void __launch_bounds__(NT) simt_fwd_kernel(FwdArgs a) {
 #pragma unroll
   for (int m = 0; m < NM; ++m) acc[m] = 0.f;
   float mrow = -INFINITY, lrow = 0.f;
-  for (int j0 = 0; j0 < N; j0 += BC) {
+  const int jend = a.causal ? min(N, i0 + BR) : N;   // causal: keys up to the block's last row
+  for (int j0 = 0; j0 < jend; j0 += BC) {
     __syncthreads();
     load_rows<T, D>(sK, K, j0, N);
     load_rows<T, D>(sV, V, j0, N);
@@ -93,7 +95,8 @@ __global__ void __launch_bounds__(NT) simt_fwd_kernel(FwdArgs a) {
     float tmax = -INFINITY;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      s[m] = (j0 + 4 * q + m < N) ? a.tau * s[m] : -INFINITY;
+      const int jj = j0 + 4 * q + m;
+      s[m] = (jj < N && (!a.causal || jj <= i)) ? a.tau * s[m] : -INFINITY;
       tmax = fmaxf(tmax, s[m]);
     }
     const float mnew = fmaxf(mrow, row_max8(tmax));
@@ -158,7 +161,7 @@ __global__ void __launch_bounds__(NT) simt_bwd_dq_kernel(BwdArgs a) {
   float acc[NM];
 #pragma unroll
   for (int m = 0; m < NM; ++m) acc[m] = 0.f;
-  for (int j0 = 0; j0 < N; j0 += BC) {
+  for (int j0 = 0; j0 < (a.causal ? min(N, i0 + BR) : N); j0 += BC) {
     __syncthreads();
     load_rows<T, D>(sK, K, j0, N);
     load_rows<T, D>(sV, V, j0, N);
@@ -174,7 +177,7 @@ __global__ void __launch_bounds__(NT) simt_bwd_dq_kernel(BwdArgs a) {
     }
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      const bool ok = (i < N) && (j0 + 4 * q + m < N);
+      const bool ok = (i < N) && (j0 + 4 * q + m < N) && (!a.causal || j0 + 4 * q + m <= i);
       const float p = ok ? expf(a.tau * s[m] - Lr) : 0.f;
       odS[r * LO + 4 * q + m] = p * (dp[m] - Dr);
     }
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(NT) simt_bwd_dkdv_kernel(BwdArgs a) {
   float accK[NM], accV[NM];
 #pragma unroll
   for (int m = 0; m < NM; ++m) accK[m] = accV[m] = 0.f;
-  for (int c0 = 0; c0 < N; c0 += BC) {
+  for (int c0 = a.causal ? j0 : 0; c0 < N; c0 += BC) {   // causal: queries from the block's first key
     __syncthreads();
     load_rows<T, D>(sQ, Q, c0, N);
     load_rows<T, D>(sdO, dO, c0, N);
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(NT) simt_bwd_dkdv_kernel(BwdArgs a) {
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int cc = 4 * q + m;
-      const bool ok = (j < N) && (c0 + cc < N);
+      const bool ok = (j < N) && (c0 + cc < N) && (!a.causal || c0 + cc >= j);
       const float p = ok ? expf(a.tau * s[m] - sL[cc]) : 0.f;
       oP[r * LO + cc] = p;
       odS[r * LO + cc] = p * (dp[m] - sD[cc]);
@@ -308,7 +311,7 @@ __global__ void __launch_bounds__(NT) simt_bob_pass1_kernel(BobArgs a) {
 #pragma unroll
   for (int m = 0; m < NM; ++m) U1[m] = U2[m] = Wa[m] = Y[m] = 0.f;
   float alpha_p = 0.f, ex_p = 0.f;
-  for (int j0 = 0; j0 < N; j0 += BC) {
+  for (int j0 = 0; j0 < (a.causal ? min(N, i0 + BR) : N); j0 += BC) {
     __syncthreads();
     load_rows<T, D>(sK, K, j0, N);
     load_rows<T, D>(sV, V, j0, N);
@@ -332,7 +335,7 @@ __global__ void __launch_bounds__(NT) simt_bob_pass1_kernel(BobArgs a) {
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int jj = 4 * q + m;
-      const bool ok = (i < N) && (j0 + jj < N);
+      const bool ok = (i < N) && (j0 + jj < N) && (!a.causal || j0 + jj <= i);
       const float p = ok ? expf(a.tau * s[m] - Lr) : 0.f;
       const float b = a.tau * bb[m];
       const float t = dp[m] - Dr;
@@ -416,7 +419,7 @@ __global__ void __launch_bounds__(NT) simt_bob_pass2_kernel(BobArgs a) {
   float AK[NM], AV[NM];
 #pragma unroll
   for (int m = 0; m < NM; ++m) AK[m] = AV[m] = 0.f;
-  for (int c0 = 0; c0 < N; c0 += BC) {
+  for (int c0 = a.causal ? j0 : 0; c0 < N; c0 += BC) {   // causal: queries from the block's first key
     __syncthreads();
     load_rows<T, D>(sQ, Q, c0, N);
     load_rows<T, D>(sdO, dO, c0, N);
@@ -451,7 +454,7 @@ __global__ void __launch_bounds__(NT) simt_bob_pass2_kernel(BobArgs a) {
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int ii = 4 * q + m;
-      const bool ok = (j < N) && (c0 + ii < N);
+      const bool ok = (j < N) && (c0 + ii < N) && (!a.causal || c0 + ii >= j);
       const float p = ok ? expf(a.tau * s[m] - sL[ii]) : 0.f;
       const float t = dp[m] - sD[ii];
       const float bp = fmaf(a.tau, bb[m], -sA[ii]);

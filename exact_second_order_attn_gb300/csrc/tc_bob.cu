@@ -61,6 +61,7 @@ struct P1Params {
   float *gQ, *gdO, *ws;
   int N;
   float tau;
+  int causal;
   unsigned int* err;
   unsigned long long wait_ns;
   int stall;
@@ -74,6 +75,7 @@ struct P2Params {
   float *gK, *gV;
   int N;
   float tau;
+  int causal;
   unsigned int* err;
   unsigned long long wait_ns;
   int stall;
@@ -97,7 +99,7 @@ __device__ __forceinline__ void load_tile2(const CUtensorMap* m0, const CUtensor
 template <int D_>
 struct PassU1 {
   using Params = P1Params;
-  static constexpr bool SPLIT = false;
+  static constexpr bool SPLIT = false, ROWS = true;
   static constexpr int D = D_, DC = D / 64, T = 32;
   static constexpr bool kWide = D == 128;
   static constexpr int TRES = kWide ? 2 : 3;            // Q, UQ (, dO)
@@ -170,6 +172,7 @@ struct PassU1 {
     w.alpha = 0.f;
     w.ex = 0.f;
   }
+  template <bool MASK>
   __device__ static bool ew_tile(Row& w, const Params& p, const TileArgs& a, const TileSync& s, int r) {
     const float sc = p.tau * kLog2e;
     uint32_t wdS[16], wX[16];
@@ -183,7 +186,8 @@ struct PassU1 {
         float ds[2], x[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float pe = ex2(fmaf(S[j + e], sc, w.nL));
+          const int col = q * 16 + j + e;   // tile column (key)
+          const float pe = (!MASK || (col >= a.lo && col <= a.hi)) ? ex2(fmaf(S[j + e], sc, w.nL)) : 0.f;
           const float be = p.tau * B[j + e];
           const float te = dP[j + e] - w.Di;
           w.alpha = fmaf(pe, be, w.alpha);
@@ -230,7 +234,7 @@ struct PassU1 {
 template <int D_>
 struct PassZ {
   using Params = P1Params;
-  static constexpr bool SPLIT = false;
+  static constexpr bool SPLIT = false, ROWS = true;
   static constexpr int D = D_, DC = D / 64, T = 64, BLK = T * 128;
   static constexpr int RES = 0, TRES = 2;   // Q, dO
   static constexpr int ACH = BLK, BCH = BLK;
@@ -284,6 +288,7 @@ struct PassZ {
     w.alpha = p.ws[2 * vo];                              // row totals of the U1 sweep
     w.ex = fmaf(-w.Di, w.alpha, p.ws[2 * vo + 1]);       // EX = E - D alpha
   }
+  template <bool MASK>
   __device__ static bool ew_tile(Row& w, const Params& p, const TileArgs& a, const TileSync& s, int r) {
     const float sc = p.tau * kLog2e;
     uint32_t wg[T / 2];
@@ -297,7 +302,8 @@ struct PassZ {
         float g[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float pe = ex2(fmaf(S[j + e], sc, w.nL));
+          const int col = q * 16 + j + e;   // tile column (key)
+          const float pe = (!MASK || (col >= a.lo && col <= a.hi)) ? ex2(fmaf(S[j + e], sc, w.nL)) : 0.f;
           g[e] = pe * fmaf(w.alpha, dP[j + e] - w.Di, w.ex);   // EX P + alpha dS
         }
         wg[q * 8 + j / 2] = pack_bf16x2(g[0], g[1]);
@@ -340,7 +346,7 @@ struct PassZ {
 template <int D_>
 struct PassY {
   using Params = P1Params;
-  static constexpr bool SPLIT = false;
+  static constexpr bool SPLIT = false, ROWS = true;
   static constexpr int D = D_, DC = D / 64, T = D == 128 ? 32 : 64, BLK = T * 128;
   static constexpr int RES = 0, TRES = 2;   // Q, UQ
   static constexpr int ACH = 2 * BLK, BCH = 2 * BLK;
@@ -390,32 +396,32 @@ struct PassY {
     w.nL = -p.L[(size_t)head * p.N + blk0 + r] * kLog2e;
     w.alpha = 0.f;
   }
+  template <bool MASK>
   __device__ static bool ew_tile(Row& w, const Params& p, const TileArgs& a, const TileSync& s, int) {
     const float sc = p.tau * kLog2e;
-    uint32_t wP[T / 2], wPB[T / 2];
+    // operands written chunk by chunk (see the dK/dV kernel)
+    if (!s.acquire_ops()) return false;
 #pragma unroll
     for (int q = 0; q < T / 16; ++q) {
       float S[16], B[16];
       tmem_ld16x2(a.sc + q * 16, a.sc + T + q * 16, S, B);
       if (q == T / 16 - 1) s.release_scores();
+      uint32_t wP[8], wPB[8];
 #pragma unroll
       for (int j = 0; j < 16; j += 2) {
         float pv[2], pb[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          pv[e] = ex2(fmaf(S[j + e], sc, w.nL));
+          const int col = q * 16 + j + e;   // tile column (key)
+          pv[e] = (!MASK || (col >= a.lo && col <= a.hi)) ? ex2(fmaf(S[j + e], sc, w.nL)) : 0.f;
           pb[e] = pv[e] * (p.tau * B[j + e]);
           w.alpha += pb[e];
         }
-        wP[q * 8 + j / 2] = pack_bf16x2(pv[0], pv[1]);
-        wPB[q * 8 + j / 2] = pack_bf16x2(pb[0], pb[1]);
+        wP[j / 2] = pack_bf16x2(pv[0], pv[1]);
+        wPB[j / 2] = pack_bf16x2(pb[0], pb[1]);
       }
-    }
-    if (!s.acquire_ops()) return false;
-#pragma unroll
-    for (int c = 0; c < T / 32; ++c) {
-      tmem_st16_nowait(a.ops + 16 * c, wP + 16 * c);
-      tmem_st16_nowait(a.ops + T / 2 + 16 * c, wPB + 16 * c);
+      tmem_st8_nowait(a.ops + 8 * q, wP);
+      tmem_st8_nowait(a.ops + T / 2 + 8 * q, wPB);
     }
     s.publish_ops();
     return true;
@@ -449,6 +455,7 @@ struct PassY {
 template <int D_>
 struct Pass2 {
   using Params = P2Params;
+  static constexpr bool ROWS = false;
   static constexpr int D = D_, DC = D / 64, T = kT;
   static constexpr bool kAllTmem = D == 64;        // V, UV also in TMEM; operands in TMEM
   static constexpr int TRES = kAllTmem ? 4 : 2;    // K, UK (, V, UV)
@@ -540,11 +547,13 @@ struct Pass2 {
   // between the warpgroups measured slower here).
   static constexpr bool SPLIT = false;
   static constexpr int NC = SPLIT ? T / 2 : T;
+  template <bool MASK>
   __device__ static bool ew_tile(Row&, const Params& p, const TileArgs& a, const TileSync& s, int r) {
     const float sc = p.tau * kLog2e;
     const float* vL = a.vec + a.c0;
     const float* vD = a.vec + T + a.c0;
     const float2* vAE = reinterpret_cast<const float2*>(a.vec + 2 * T) + a.c0;
+    // one score buffer: its release comes first, the operands are taken after
     uint32_t wdS[NC / 2], wGs[NC / 2], wGd[NC / 2];
 #pragma unroll
     for (int q = 0; q < NC / 16; ++q) {
@@ -560,7 +569,8 @@ struct Pass2 {
           const int ii = q * 16 + j + e;   // query column (relative to a.c0)
           const float Dq = vD[ii];
           const float2 ae = vAE[ii];
-          const float pe = ex2(fmaf(S[j + e], sc, -vL[ii] * kLog2e));
+          const int col = a.c0 + ii;         // tile column (query)
+          const float pe = (!MASK || (col >= a.lo && col <= a.hi)) ? ex2(fmaf(S[j + e], sc, -vL[ii] * kLog2e)) : 0.f;
           const float te = dP[j + e] - Dq;
           const float bp = fmaf(p.tau, B[j + e], -ae.x);
           dsv[e] = pe * te;
@@ -574,19 +584,19 @@ struct Pass2 {
       }
     }
     if (!s.acquire_ops()) return false;
-    if (kAllTmem) {
-      const uint32_t o = a.ops + a.c0 / 2;
 #pragma unroll
-      for (int c = 0; c < NC / 16; ++c) {
-        tmem_st8_nowait(o + 8 * c, wdS + 8 * c);
-        tmem_st8_nowait(o + 16 + 8 * c, wGs + 8 * c);
-        tmem_st8_nowait(o + 32 + 8 * c, wGd + 8 * c);
+    for (int q = 0; q < NC / 16; ++q) {
+      if (kAllTmem) {
+        const uint32_t o = a.ops + (a.c0 + q * 16) / 2;
+        tmem_st8_nowait(o, wdS + 8 * q);
+        tmem_st8_nowait(o + 16, wGs + 8 * q);
+        tmem_st8_nowait(o + 32, wGd + 8 * q);
+      } else {
+        const int col = 32 * (int)a.h + a.c0 + q * 16;
+        write_op_cols<8>(a.ops, (uint32_t)r, col, wdS + 8 * q);
+        write_op_cols<8>(a.ops + kChunk, (uint32_t)r, col, wGs + 8 * q);
+        write_op_cols<8>(a.ops + 2 * kChunk, (uint32_t)r, col, wGd + 8 * q);
       }
-    } else {
-      const int col = 32 * (int)a.h + a.c0;
-      write_op_cols<NC / 2>(a.ops, (uint32_t)r, col, wdS);
-      write_op_cols<NC / 2>(a.ops + kChunk, (uint32_t)r, col, wGs);
-      write_op_cols<NC / 2>(a.ops + 2 * kChunk, (uint32_t)r, col, wGd);
     }
     s.publish_ops();
     return true;
@@ -612,7 +622,7 @@ struct Pass2 {
 // ===========================================================================
 template <class Op>
 cudaError_t launch(const char* name, const typename Op::Params& prm, dim3 grid, cudaStream_t s) {
-  auto kernel = tile_kernel<Op>;
+  auto kernel = prm.causal ? tile_kernel<Op, true> : tile_kernel<Op, false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Op::SMEM);
   if (e != cudaSuccess) return e;
   prof_begin(s, name);
@@ -642,6 +652,7 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   p1.ws = a.ws;
   p1.N = N;
   p1.tau = a.tau;
+  p1.causal = a.causal;
   p1.err = c.err;
   p1.wait_ns = c.wait_ns;
   p1.stall = c.stall;
@@ -667,6 +678,7 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   p2.gV = a.gV;
   p2.N = N;
   p2.tau = a.tau;
+  p2.causal = a.causal;
   p2.err = c.err;
   p2.wait_ns = c.wait_ns;
   p2.stall = c.stall;

@@ -35,6 +35,7 @@ struct DqParams {
   float *dQ, *D;
   int N;
   float tau;
+  int causal;
   unsigned int* err;
   unsigned long long wait_ns;
   int stall;
@@ -47,7 +48,7 @@ struct DqParams {
 template <int D_>
 struct DqOp {
   using Params = DqParams;
-  static constexpr bool SPLIT = false;
+  static constexpr bool SPLIT = false, ROWS = true;
   static constexpr int D = D_, DC = D / 64, T = 64, BLK = T * 128;
   static constexpr int RES = 0, TRES = 2;
   static constexpr int ACH = BLK, BCH = BLK;
@@ -121,6 +122,7 @@ struct DqOp {
     w.Di = Di;
     w.nL = -p.L[vo] * tile::kLog2e;
   }
+  template <bool MASK>
   __device__ static bool ew_tile(Row& w, const Params& p, const tile::TileArgs& a, const tile::TileSync& s, int r) {
     const float sc = p.tau * tile::kLog2e;
     uint32_t wd[T / 2];
@@ -131,7 +133,9 @@ struct DqOp {
       if (q == T / 16 - 1) s.release_scores();
 #pragma unroll
       for (int j = 0; j < 16; j += 2) {
-        const float p0 = tile::ex2(fmaf(S[j], sc, w.nL)), p1 = tile::ex2(fmaf(S[j + 1], sc, w.nL));
+        const int c = q * 16 + j;   // tile column (key)
+        const float p0 = (!MASK || (c >= a.lo && c <= a.hi)) ? tile::ex2(fmaf(S[j], sc, w.nL)) : 0.f;
+        const float p1 = (!MASK || (c + 1 >= a.lo && c + 1 <= a.hi)) ? tile::ex2(fmaf(S[j + 1], sc, w.nL)) : 0.f;
         wd[q * 8 + j / 2] = pack_bf16x2(p0 * (dP[j] - w.Di), p1 * (dP[j + 1] - w.Di));
       }
     }
@@ -166,6 +170,7 @@ struct DkvParams {
   float *dK, *dV;
   int N;
   float tau;
+  int causal;
   unsigned int* err;
   unsigned long long wait_ns;
   int stall;
@@ -177,6 +182,7 @@ struct DkvParams {
 template <int D_>
 struct DkvOp {
   using Params = DkvParams;
+  static constexpr bool ROWS = false;
   static constexpr int D = D_, DC = D / 64, T = 64, BLK = T * 128;
   static constexpr int RES = 0, TRES = 2;
   static constexpr int ACH = 2 * BLK, VEC_OFF = DC * ACH;
@@ -227,28 +233,43 @@ struct DkvOp {
   // T / 2 (starting at a.c0) when both warpgroups share the one buffer.
   static constexpr bool SPLIT = NBUF == 1;
   static constexpr int NC = SPLIT ? T / 2 : T;
+  template <bool MASK>
   __device__ static bool ew_tile(Row&, const Params& p, const tile::TileArgs& a, const tile::TileSync& s, int r) {
     const float sc = p.tau * tile::kLog2e;
     const float* vL = a.vec + a.c0;
     const float* vD = a.vec + T + a.c0;
-    uint32_t wP[NC / 2], wd[NC / 2];
+    // With one score buffer its release is on the critical path, so the
+    // operand tiles are taken only after all scores are read; with two, they
+    // are taken first and each 16-column chunk is written as soon as it is
+    // computed (fewer live registers).
+    constexpr bool kEarly = NBUF > 1;
+    if (kEarly && !s.acquire_ops()) return false;
+    uint32_t wP[kEarly ? 8 : NC / 2], wd[kEarly ? 8 : NC / 2];
 #pragma unroll
     for (int q = 0; q < NC / 16; ++q) {
       float S[16], dP[16];
       tmem_ld16x2(a.sc + a.c0 + q * 16, a.sc + T + a.c0 + q * 16, S, dP);
       if (q == NC / 16 - 1) s.release_scores();
+      const int o = kEarly ? 0 : q * 8;
 #pragma unroll
       for (int c = 0; c < 16; c += 2) {
-        const int ii = q * 16 + c;
-        const float p0 = tile::ex2(fmaf(S[c], sc, -vL[ii] * tile::kLog2e));
-        const float p1 = tile::ex2(fmaf(S[c + 1], sc, -vL[ii + 1] * tile::kLog2e));
-        wP[q * 8 + c / 2] = pack_bf16x2(p0, p1);
-        wd[q * 8 + c / 2] = pack_bf16x2(p0 * (dP[c] - vD[ii]), p1 * (dP[c + 1] - vD[ii + 1]));
+        const int ii = q * 16 + c, col = a.c0 + ii;   // tile column (query)
+        const float p0 = (!MASK || (col >= a.lo && col <= a.hi)) ? tile::ex2(fmaf(S[c], sc, -vL[ii] * tile::kLog2e)) : 0.f;
+        const float p1 =
+            (!MASK || (col + 1 >= a.lo && col + 1 <= a.hi)) ? tile::ex2(fmaf(S[c + 1], sc, -vL[ii + 1] * tile::kLog2e)) : 0.f;
+        wP[o + c / 2] = pack_bf16x2(p0, p1);
+        wd[o + c / 2] = pack_bf16x2(p0 * (dP[c] - vD[ii]), p1 * (dP[c + 1] - vD[ii + 1]));
+      }
+      if (kEarly) {
+        tile::write_op_cols<8>(a.ops + a.h * tile::kChunk, (uint32_t)r, a.c0 + q * 16, wP);
+        tile::write_op_cols<8>(a.ops + (2 + a.h) * tile::kChunk, (uint32_t)r, a.c0 + q * 16, wd);
       }
     }
-    if (!s.acquire_ops()) return false;
-    tile::write_op_cols<NC / 2>(a.ops + a.h * tile::kChunk, (uint32_t)r, a.c0, wP);
-    tile::write_op_cols<NC / 2>(a.ops + (2 + a.h) * tile::kChunk, (uint32_t)r, a.c0, wd);
+    if (!kEarly) {
+      if (!s.acquire_ops()) return false;
+      tile::write_op_cols<NC / 2>(a.ops + a.h * tile::kChunk, (uint32_t)r, a.c0, wP);
+      tile::write_op_cols<NC / 2>(a.ops + (2 + a.h) * tile::kChunk, (uint32_t)r, a.c0, wd);
+    }
     s.publish_ops();
     return true;
   }
@@ -293,11 +314,13 @@ cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
   q.D = a.D;
   q.N = a.N;
   q.tau = a.tau;
+  q.causal = a.causal;
   q.err = c.err;
   q.wait_ns = c.wait_ns;
   q.stall = c.stall;
   const dim3 grid(a.N / kM, a.BH);
-  cudaError_t e = launch("attn_bwd_dq", tile::tile_kernel<DqOp<D>>, DqOp<D>::SMEM, tile::kThreads, grid, q, s);
+  cudaError_t e = launch("attn_bwd_dq", a.causal ? tile::tile_kernel<DqOp<D>, true> : tile::tile_kernel<DqOp<D>, false>,
+                         DqOp<D>::SMEM, tile::kThreads, grid, q, s);
   if (e != cudaSuccess) return e;
   DkvParams k;
   if (!make_bf16_map(&k.mQ, a.Q, a.BH, a.N, D, DkvOp<D>::T) || !make_bf16_map(&k.mdO, a.dO, a.BH, a.N, D, DkvOp<D>::T))
@@ -310,10 +333,12 @@ cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
   k.dV = a.dV;
   k.N = a.N;
   k.tau = a.tau;
+  k.causal = a.causal;
   k.err = c.err;
   k.wait_ns = c.wait_ns;
   k.stall = c.stall;
-  return launch("attn_bwd_dkdv", tile::tile_kernel<DkvOp<D>>, DkvOp<D>::SMEM, tile::kThreads, grid, k, s);
+  return launch("attn_bwd_dkdv", a.causal ? tile::tile_kernel<DkvOp<D>, true> : tile::tile_kernel<DkvOp<D>, false>,
+                DkvOp<D>::SMEM, tile::kThreads, grid, k, s);
 }
 
 }  // namespace

@@ -44,6 +44,7 @@ struct FwdParams {
   float *O, *L;
   int N;
   float tau;
+  int causal;
   unsigned int* err;
   unsigned long long wait_ns;
   int stall;
@@ -70,15 +71,75 @@ struct Ctrl {
   int abort_flag;
 };
 
-template <int D>
+// One tile of the softmax of one row (this thread's TMEM lane): pass 1 finds
+// the tile's row max over columns 0..lim, a lazy rescale of O and l follows
+// when the max grew by more than 2^8 (after the block's previous P V product
+// has landed), pass 2 writes P = 2^(x - m) as bf16 over the first 64 columns
+// of S (chunk c writes columns 16c..16c+15, all already read) and sums it
+// into ls.  MASK = false skips the column test (tiles below the diagonal).
+template <int D, bool MASK>
+__device__ __forceinline__ bool softmax_tile(uint32_t s_col, uint32_t o_col, int lim, float sc, float& m, float& l,
+                                             float& ls, uint64_t& o_done, int t, const Waiter& wt) {
+  float mt = -INFINITY;
+#pragma unroll 1
+  for (int c = 0; c < kKT / 32; ++c) {
+    float s[32];
+    tmem_ld32(s_col + 32 * c, s);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) mt = fmaxf(mt, (!MASK || 32 * c + j <= lim) ? s[j] : -INFINITY);
+  }
+  mt *= sc;
+  if (__any_sync(0xffffffffu, mt > m + kRescale)) {
+    const float mn = fmaxf(m, mt);
+    if (t > 0) {
+      const float scale = tile::ex2(m - mn);
+      // the previous P V product of this block must have landed
+      if (!mbar_wait(&o_done, (t - 1) & 1, wt)) return false;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        float o[16];
+        tmem_ld16(o_col + c0, o);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(o[e] * scale);
+        tmem_st16_nowait(o_col + c0, w);
+      }
+      tmem_st_wait();
+      l *= scale;
+    }
+    m = mn;
+  }
+#pragma unroll 1
+  for (int c = 0; c < kKT / 32; ++c) {
+    float s[32];
+    tmem_ld32(s_col + 32 * c, s);
+    uint32_t w[16];
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const float p0 = (!MASK || 32 * c + j <= lim) ? tile::ex2(fmaf(s[j], sc, -m)) : 0.f;
+      const float p1 = (!MASK || 32 * c + j + 1 <= lim) ? tile::ex2(fmaf(s[j + 1], sc, -m)) : 0.f;
+      ls += p0 + p1;
+      w[j / 2] = pack_bf16x2(p0, p1);
+    }
+    tmem_st16_nowait(s_col + 16 * c, w);
+  }
+  return true;
+}
+
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ Ctrl ctrl;
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int row0 = blockIdx.x * 2 * kM, head = blockIdx.y;
+  // causal: block X streams the key tiles up to its diagonal (tile
+  // row0 / 128 + X), so the last pairs of blocks do the most work and run first
+  const int pair = CAUSAL ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  const int row0 = pair * 2 * kM, head = blockIdx.y;
   const int nblk = (row0 + kM < p.N) ? 2 : 1;   // block B exists unless N is an odd multiple of 128
-  const int nt = p.N / kKT;
+  const int ntx[2] = {CAUSAL ? row0 / kKT + 1 : p.N / kKT, CAUSAL ? row0 / kKT + 2 : p.N / kKT};
+  const int nt = ntx[nblk - 1];                 // key tiles the CTA streams
 
   if (tid == 0) {
     ctrl.abort_flag = 0;
@@ -163,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc(const __grid_constant
         const uint32_t k_lo = desc_lo(sm0 + C::K_OFF + sk * C::TILE, 16);
         ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.k_full[sk], (t / C::NK) & 1, wt));
         for (int x = 0; ok && x < nblk; ++x) {
+          if (t >= ntx[x]) continue;
           if (t > 0) ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.o_done[x], (t - 1) & 1, wt));
           if (!ok) break;
           tc_fence_after();
@@ -187,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc(const __grid_constant
         const uint32_t v_mn = desc_lo(sm0 + C::V_OFF + sv * C::TILE, kChunk);
         ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.v_full[sv], (t / C::NV) & 1, wt));
         for (int x = 0; ok && x < nblk; ++x) {
+          if (t >= ntx[x]) continue;
           ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.p_full[x], t & 1, wt));
           if (!ok) break;
           tc_fence_after();
@@ -210,63 +273,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc(const __grid_constant
     const float sc = p.tau * kLog2e;
     float m = -INFINITY, l = 0.f;
     bool ok = live && x < nblk;
-    for (int t = 0; t < nt && ok; ++t) {
+    const int ntb = ntx[x < nblk ? x : 0];
+    for (int t = 0; t < ntb && ok; ++t) {
       if (!mbar_wait(&ctrl.s_full[x], t & 1, wt)) { ok = false; break; }
       tc_fence_after();
-      // pass 1: tile row max
-      float mt = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < kKT / 32; ++c) {
-        float s[32];
-        tmem_ld32(s_col + 32 * c, s);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) mt = fmaxf(mt, s[j]);
-      }
-      mt *= sc;
-      if (__any_sync(0xffffffffu, mt > m + kRescale)) {
-        const float mn = fmaxf(m, mt);
-        if (t > 0) {
-          const float scale = tile::ex2(m - mn);
-          // the previous P V product of this block must have landed
-          if (!mbar_wait(&ctrl.o_done[x], (t - 1) & 1, wt)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t ob = tb + lane + x * D;
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 16) {
-            float o[16];
-            tmem_ld16(ob + c0, o);
-            uint32_t w[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(o[e] * scale);
-            tmem_st16_nowait(ob + c0, w);
-          }
-          tmem_st_wait();
-          l *= scale;
-        }
-        m = mn;
-      }
-      // pass 2: P = 2^(x - m) as bf16 over the first 64 columns of S_X; chunk
-      // c writes columns 16c..16c+15, all already read (c/2 <= c)
+      // this row may see tile columns 0..lim (causal: keys up to its own index);
+      // the masked variant runs only on a block's diagonal tile
+      const int lim = CAUSAL ? row0 + x * kM + r - t * kKT : kKT - 1;
       float ls = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < kKT / 32; ++c) {
-        float s[32];
-        tmem_ld32(s_col + 32 * c, s);
-        uint32_t w[16];
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float p0 = tile::ex2(fmaf(s[j], sc, -m)), p1 = tile::ex2(fmaf(s[j + 1], sc, -m));
-          ls += p0 + p1;
-          w[j / 2] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16_nowait(s_col + 16 * c, w);
-      }
+      const bool fine = (CAUSAL && __any_sync(0xffffffffu, lim < kKT - 1))
+                            ? softmax_tile<D, CAUSAL>(s_col, tb + lane + x * D, lim, sc, m, l, ls, ctrl.o_done[x], t, wt)
+                            : softmax_tile<D, false>(s_col, tb + lane + x * D, lim, sc, m, l, ls, ctrl.o_done[x], t, wt);
+      if (!fine) { ok = false; break; }
       l += ls;
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&ctrl.p_full[x]);
     }
-    if (ok && mbar_wait(&ctrl.o_done[x], (nt - 1) & 1, wt)) {
+    if (ok && mbar_wait(&ctrl.o_done[x], (ntb - 1) & 1, wt)) {
       tc_fence_after();
       const int i = row0 + x * kM + r;
       const size_t ro = ((size_t)head * p.N + i) * D;
@@ -300,10 +324,11 @@ cudaError_t fwd_d(const FwdArgs& a, const DevCtx& c, cudaStream_t s) {
   p.L = a.L;
   p.N = a.N;
   p.tau = a.tau;
+  p.causal = a.causal;
   p.err = c.err;
   p.wait_ns = c.wait_ns;
   p.stall = c.stall;
-  auto kernel = attn_fwd_tc<D>;
+  auto kernel = a.causal ? attn_fwd_tc<D, true> : attn_fwd_tc<D, false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((a.N + 2 * kM - 1) / (2 * kM), a.BH);

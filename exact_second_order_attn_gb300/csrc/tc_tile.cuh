@@ -182,11 +182,14 @@ struct TileArgs {
   const float* vec;    // ring-A vectors of the tile (shared memory) or nullptr
   uint32_t ops;        // SS: shared address of operand tile 0; TS: TMEM address of the half's first column
   uint32_t h;          // operand half (SS: columns 32h..32h+31 of each [128][64] operand tile)
-  int t;               // tile index
+  int t;               // streamed tile index (data)
   int c0;              // first tile column this warpgroup handles (0, or T/2 when the columns are split)
+  int lo, hi;          // tile columns [lo, hi] this thread's row may see (causal mask; else [0, T-1])
 };
 
-template <class Op>
+// CAUSAL is a compile-time choice, so the full-attention kernels carry no
+// mask code; the host launches the instantiation that matches p.causal.
+template <class Op, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant__ typename Op::Params p) {
   static_assert(Op::NSB == 0 || Op::NSB == Op::NSA, "ring B stages pair with ring A stages");
   static_assert(Op::NBUF < Op::NSA, "the MMA order needs more stages than score buffers");
@@ -196,8 +199,14 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ Ctrl ctrl;
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int blk0 = blockIdx.x * kM, head = blockIdx.y;
-  const int nt = p.N / Op::T;
+  // Causal: a row block (ROWS: resident queries) streams the key tiles up to
+  // its diagonal, a column block (resident keys) the query tiles from its
+  // diagonal.  Row blocks then run the heaviest (last) blocks first.
+  const int blk = (Op::ROWS && CAUSAL) ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  const int blk0 = blk * kM, head = blockIdx.y;
+  const int t_begin = (CAUSAL && !Op::ROWS) ? blk0 / Op::T : 0;
+  const int t_end = (CAUSAL && Op::ROWS) ? (blk0 + kM) / Op::T : p.N / Op::T;
+  const int nt = t_end - t_begin;   // loop steps; step t streams tile t_begin + t
   uint8_t* res = smem;
   uint8_t* ring_a = res + Op::RES;
   uint8_t* ring_b = ring_a + Op::NSA * Op::SA;
@@ -263,8 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
         }
         if (p.stall && t == 0) continue;  // test hook: nothing will fill this stage
         mbar_arrive_expect_tx(&ctrl.a_full[sa], Op::SA_TX + (Op::NSB > 0 ? Op::SB_TX : 0));
-        Op::load_a(p, ring_a + sa * Op::SA, &ctrl.a_full[sa], t, head);
-        if constexpr (Op::NSB > 0) Op::load_b(p, ring_b + sa * Op::SB, &ctrl.a_full[sa], t, head);
+        Op::load_a(p, ring_a + sa * Op::SA, &ctrl.a_full[sa], t_begin + t, head);
+        if constexpr (Op::NSB > 0) Op::load_b(p, ring_b + sa * Op::SB, &ctrl.a_full[sa], t_begin + t, head);
         FBOB_STAMP(7, t);
         ia = t + 1;
       }
@@ -390,9 +399,18 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
       ta.vec = Op::VEC ? reinterpret_cast<const float*>(ring_a + sa * Op::SA + Op::VEC_OFF) : nullptr;
       ta.ops = Op::TS ? (tb + lane + Op::OP_COL + (uint32_t)q * Op::OP_HALF) : smem_u32(ops);
       ta.h = (uint32_t)q;
-      ta.t = t;
+      ta.t = t_begin + t;
       ta.c0 = kSplit ? g * (Op::T / 2) : 0;
-      ok = Op::ew_tile(row, p, ta, sync, r);
+      // causal: column c of the tile is key / query (t_begin + t) T + c
+      const int diag = blk0 + r - ta.t * Op::T;   // this row's own index, as a tile column
+      ta.lo = (CAUSAL && !Op::ROWS) ? diag : 0;
+      ta.hi = (CAUSAL && Op::ROWS) ? diag : Op::T - 1;
+      // tiles that cross the diagonal (causal) take the masked variant; the
+      // vote keeps the choice warp-uniform
+      if (CAUSAL && __any_sync(0xffffffffu, ta.lo > 0 || ta.hi < Op::T - 1))
+        ok = Op::template ew_tile<CAUSAL>(row, p, ta, sync, r);
+      else
+        ok = Op::template ew_tile<false>(row, p, ta, sync, r);
       FBOB_STAMP(6, t);
 
     }

@@ -33,7 +33,7 @@
  * - Every pointer must be 16-byte aligned and tensors must not overlap an
  *   output of the same call.
  * - Supported: d in {64, 128}; any N >= 1 for fp32 inputs; N a multiple of
- *   128 for bf16 inputs; causal = 0.  B*H*N == 0 is a valid empty problem
+ *   128 for bf16 inputs; causal or not.  B*H*N == 0 is a valid empty problem
  *   (returns FBOB_OK, launches nothing).
  * - Argument problems are reported BEFORE any launch (nothing is launched on
  *   error).  A failed launch returns FBOB_ERR_CUDA.  Kernels never trap: a
@@ -74,7 +74,8 @@ typedef struct {
   int B, H, N, d;
   float tau;                  /* score scale, S = tau Q K^T; finite, nonzero  */
   int dtype;                  /* fbob_dtype of Q, K, V, dO, UQ, UK, UV        */
-  int causal;                 /* must be 0 (non-causal)                       */
+  int causal;                 /* 0: full attention; nonzero: causal, query i  */
+                              /* attends to keys j <= i                       */
 } fbob_problem;
 
 /*

@@ -26,15 +26,15 @@ def to_dev(inputs, device="cuda"):
     return {k: v.to(device) for k, v in inputs.items()}
 
 
-def run_chain(w, inp=None, stream=None):
+def run_chain(w, inp=None, stream=None, causal=False):
     """Run fwd, bwd and BoB on the GPU; return a dict of CPU float64 arrays."""
     if inp is None:
         inp = attn_inputs.make_inputs(w)
     x = to_dev(inp)
-    O, L = fb.attn_fwd(x["Q"], x["K"], x["V"], w.tau, stream=stream)
-    dQ, dK, dV, D = fb.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], L, w.tau, stream=stream)
+    O, L = fb.attn_fwd(x["Q"], x["K"], x["V"], w.tau, stream=stream, causal=causal)
+    dQ, dK, dV, D = fb.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], L, w.tau, stream=stream, causal=causal)
     gQ, gK, gV, gdO, ws = fb.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], L, D, x["UQ"], x["UK"], x["UV"],
-                                      w.tau, stream=stream)
+                                      w.tau, stream=stream, causal=causal)
     fb.device_status(stream)
     out = dict(O=O, L=L, dQ=dQ, dK=dK, dV=dV, D=D, gQ=gQ, gK=gK, gV=gV, gdO=gdO,
                alpha=ws[..., 0], E=ws[..., 1])
@@ -53,12 +53,12 @@ def oracle_inputs(inp, heads=None):
     return out
 
 
-def oracle_chain(x, tau):
-    O, L = orc.attn_fwd(x["Q"], x["K"], x["V"], tau)
-    dQ, dK, dV, D = orc.attn_bwd(x["Q"], x["K"], x["V"], x["dO"], tau)
+def oracle_chain(x, tau, causal=False):
+    O, L = orc.attn_fwd(x["Q"], x["K"], x["V"], tau, causal=causal)
+    dQ, dK, dV, D = orc.attn_bwd(x["Q"], x["K"], x["V"], x["dO"], tau, causal=causal)
     args = [x[k] for k in ("Q", "K", "V", "dO", "UQ", "UK", "UV")]
-    gQ, gK, gV, gdO = orc.attn_bob(*args, tau)
-    alpha, E = orc.bob_row_scalars(*args, tau)
+    gQ, gK, gV, gdO = orc.attn_bob(*args, tau, causal=causal)
+    alpha, E = orc.bob_row_scalars(*args, tau, causal=causal)
     return dict(O=O, L=L, dQ=dQ, dK=dK, dV=dV, D=D, gQ=gQ, gK=gK, gV=gV, gdO=gdO, alpha=alpha, E=E)
 
 

@@ -76,7 +76,6 @@ def call_bob(lib, p, ptrs=None, ws=0x10000, ws_bytes=None):
     ("d", 96, _lib.ERR_UNSUPPORTED),
     ("d", 0, _lib.ERR_INVALID_ARG),
     ("N", -1, _lib.ERR_INVALID_ARG),
-    ("causal", 1, _lib.ERR_UNSUPPORTED),
     ("dtype", 7, _lib.ERR_INVALID_ARG),
     ("tau", float("nan"), _lib.ERR_INVALID_ARG),
     ("tau", 0.0, _lib.ERR_INVALID_ARG),
@@ -112,6 +111,13 @@ def test_empty_problem_is_a_noop(lib):
         p = _lib.Problem(B, 4, N, 64, 0.125, _lib.BF16, 0)
         assert call_bob(lib, p, ptrs=[0] * 14, ws=0) == _lib.OK
         assert lib.fbob_attn_fwd(ctypes.byref(p), *[None] * 5, None) == _lib.OK
+
+
+def test_causal_passes_validation(lib):
+    # validation passes for both dtypes; without a GPU the first CUDA call then fails cleanly
+    for dt in (_lib.BF16, _lib.FP32):
+        p = _lib.Problem(1, 1, 256, 64, 0.125, dt, 1)
+        assert call_bob(lib, p) in (_lib.OK, _lib.ERR_CUDA)
 
 
 def test_fp32_allows_ragged_n_at_validation(lib):

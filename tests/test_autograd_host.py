@@ -26,19 +26,19 @@ def _t(a, like):
 def oracle_backend(monkeypatch):
     calls = []
 
-    def fwd(Q, K, V, tau, **_):
+    def fwd(Q, K, V, tau, causal=False, **_):
         calls.append("fwd")
-        O, L = orc.attn_fwd(Q.detach().numpy(), K.detach().numpy(), V.detach().numpy(), tau)
+        O, L = orc.attn_fwd(Q.detach().numpy(), K.detach().numpy(), V.detach().numpy(), tau, causal=causal)
         return _t(O, Q), _t(L, Q)
 
-    def bwd(Q, K, V, O, dO, L, tau, **_):
+    def bwd(Q, K, V, O, dO, L, tau, causal=False, **_):
         calls.append("bwd")
-        dQ, dK, dV, D = orc.attn_bwd(*(x.detach().numpy() for x in (Q, K, V, dO)), tau)
+        dQ, dK, dV, D = orc.attn_bwd(*(x.detach().numpy() for x in (Q, K, V, dO)), tau, causal=causal)
         return _t(dQ, Q), _t(dK, Q), _t(dV, Q), _t(D, Q)
 
-    def bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, **_):
+    def bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, causal=False, **_):
         calls.append("bob")
-        g = orc.attn_bob(*(x.detach().numpy() for x in (Q, K, V, dO, UQ, UK, UV)), tau)
+        g = orc.attn_bob(*(x.detach().numpy() for x in (Q, K, V, dO, UQ, UK, UV)), tau, causal=causal)
         return tuple(_t(a, Q) for a in g) + (None,)
 
     monkeypatch.setattr(_lib, "fbob_attn_fwd", fwd)
@@ -47,18 +47,22 @@ def oracle_backend(monkeypatch):
     return calls
 
 
-def torch_attention(Q, K, V, tau):
-    return torch.softmax(tau * Q @ K.transpose(-1, -2), dim=-1) @ V
+def torch_attention(Q, K, V, tau, causal=False):
+    S = tau * Q @ K.transpose(-1, -2)
+    if causal:
+        n = S.shape[-1]
+        S = S.masked_fill(torch.triu(torch.ones(n, n, dtype=torch.bool), diagonal=1), float("-inf"))
+    return torch.softmax(S, dim=-1) @ V
 
 
-@pytest.mark.parametrize("shape", [(1, 2, 12, 4), (2, 1, 7, 3)])
-def test_gradients_and_hvp_match_torch_double_backward(oracle_backend, shape):
+@pytest.mark.parametrize("shape,causal", [((1, 2, 12, 4), False), ((2, 1, 7, 3), False), ((1, 2, 10, 4), True)])
+def test_gradients_and_hvp_match_torch_double_backward(oracle_backend, shape, causal):
     g = torch.Generator().manual_seed(5)
     Q, K, V, W, vQ, vK, vV = (torch.randn(shape, generator=g, dtype=torch.float64) for _ in range(7))
     tau = 0.6
 
     def loss(f):
-        return lambda q, k, v: (torch.sin(f(q, k, v, tau)) * W).sum()   # a nonlinear head on O
+        return lambda q, k, v: (torch.sin(f(q, k, v, tau, causal)) * W).sum()   # a nonlinear head on O
 
     x = [t.clone().requires_grad_(True) for t in (Q, K, V)]
     g_ours = torch.autograd.grad(loss(ag.attention)(*x), x)
