@@ -10,7 +10,7 @@ Summary and Key claims: Hessian-vector products through attention for
 second-order optimisers such as Sophia-H).
 
 Exactly as in the kernels' C ABI:
-* Q, K, V are bf16 (tensor-core path, N a multiple of 128) or fp32 (any N);
+* Q, K, V are bf16 (tensor-core kernels) or fp32 (FFMA kernels), any N;
   O, dQ, dK, dV and the second-order outputs are fp32;
 * the incoming gradient of O and the cotangents of dQ, dK, dV are rounded to
   the input dtype before they reach the kernels (the kernels read them at the

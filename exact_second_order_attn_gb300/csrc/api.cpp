@@ -49,8 +49,6 @@ fbob_status check_problem(const fbob_problem* p, bool* empty) {
   if ((long long)p->N * p->d * heads > (1ll << 40))
     return fail(FBOB_ERR_UNSUPPORTED, "problem of %lld elements per tensor is too large",
                 (long long)p->N * p->d * heads);
-  if (p->dtype == FBOB_BF16 && p->N % 128 != 0 && p->N > 0)
-    return fail(FBOB_ERR_UNSUPPORTED, "bf16 inputs need N a multiple of 128 (got N=%d)", p->N);
   *empty = (heads == 0 || p->N == 0);
   return FBOB_OK;
 }

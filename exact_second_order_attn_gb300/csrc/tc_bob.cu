@@ -1,5 +1,5 @@
 // Tensor-core (tcgen05 + TMEM + TMA) kernels of the two-pass BoB for bf16
-// inputs, d in {64, 128}, N a multiple of 128, built on the tile skeleton of
+// inputs, d in {64, 128}, any N, built on the tile skeleton of
 // tc_tile.cuh.
 //
 // Source: "FlashBoB: I/O-Efficient Exact Backward-over-Backward for Softmax
@@ -108,7 +108,7 @@ struct PassU1 {
   static constexpr int SA = DC * ACH, SB = DC * BCH, SA_TX = SA, SB_TX = SB;
   static constexpr int NSA = kWide ? 5 : 8, NSB = NSA;
   static constexpr bool VEC = false, ROW_SUMS = true, TS = !kWide;
-  static constexpr int VEC_OFF = 0;
+  static constexpr int VEC_OFF = 0, NVEC = 0, VEC_SCRATCH = 0;
   static constexpr int OPS = kWide ? 2 * kChunk : 0;    // dS, X tiles; half h = columns 32h..32h+31
   static constexpr int ACC = D, SCOLS = 128, NBUF = 2;  // [S|B|dP|C]
   static constexpr int OP_HALF = 32;                    // TMEM operands dS, X
@@ -124,9 +124,10 @@ struct PassU1 {
   __device__ static void load_res(const Params& p, uint8_t* res, uint64_t* bar, int row0, int head) {
     for (int kc = 0; kc < DC; ++kc) tma_load_3d(res + kc * kChunk, &p.mdO_res, bar, kc * 64, row0, head);
   }
-  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
+  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head, bool) {
     load_tile2(&p.mK, &p.mUK, st, DC, ACH, kBlk, bar, t * T, head);
   }
+  __device__ static void fill_vec(const Params&, float*, int, int, int) {}
   __device__ static void load_b(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
     load_tile2(&p.mV, &p.mUV, st, DC, BCH, kBlk, bar, t * T, head);
   }
@@ -166,9 +167,10 @@ struct PassU1 {
     float nL, Di, alpha, ex;
   };
   __device__ static void ew_init(Row& w, const Params& p, int blk0, int r, int head) {
-    const size_t vo = (size_t)head * p.N + blk0 + r;
-    w.nL = -p.L[vo] * kLog2e;
-    w.Di = p.D[vo];
+    const bool ok = blk0 + r < p.N;   // ragged N: rows past the end are never stored
+    const size_t vo = (size_t)head * p.N + (ok ? blk0 + r : 0);
+    w.nL = ok ? -p.L[vo] * kLog2e : 0.f;
+    w.Di = ok ? p.D[vo] : 0.f;
     w.alpha = 0.f;
     w.ex = 0.f;
   }
@@ -213,16 +215,18 @@ struct PassU1 {
   __device__ static void epilogue(Row& w, const Params& p, const EpiArgs& e) {
     float alpha = w.alpha, ex = w.ex;
     if (!e.sum_rows(alpha, ex)) return;
-    const size_t vo = (size_t)e.head * p.N + e.blk0 + e.r;
+    // every lane runs the (warp-collective) TMEM loads; rows >= N store nothing
+    const bool keep = e.blk0 + e.r < p.N;
+    const size_t vo = (size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0);
     const size_t ro = vo * D;
     const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
 #pragma unroll 1
     for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
       float acc[16];
       tmem_ld16(e.tm + c0, acc);
-      store16(p.gQ + ro + c0, acc);   // U1, finished by the Z sweep
+      if (keep) store16(p.gQ + ro + c0, acc);   // U1, finished by the Z sweep
     }
-    if (e.g == 0) {
+    if (keep && e.g == 0) {
       p.ws[2 * vo] = alpha;
       p.ws[2 * vo + 1] = fmaf(w.Di, alpha, ex);
     }
@@ -241,7 +245,7 @@ struct PassZ {
   static constexpr int SA = DC * ACH, SB = DC * BCH, SA_TX = SA, SB_TX = SB;
   static constexpr int NSA = D == 128 ? 5 : 8, NSB = NSA;
   static constexpr bool VEC = false, ROW_SUMS = false, TS = D == 64;
-  static constexpr int VEC_OFF = 0;
+  static constexpr int VEC_OFF = 0, NVEC = 0, VEC_SCRATCH = 0;
   static constexpr int OPS = TS ? 0 : 2 * kChunk;
   static constexpr int ACC = D, SCOLS = 2 * T, NBUF = 2;   // [S | dP]
   static constexpr int OP_HALF = T / 2, OP_COL = ACC + NBUF * SCOLS;
@@ -252,9 +256,10 @@ struct PassZ {
 
   __device__ static const void* tres_src(const Params& p, int s) { return s == 0 ? (const void*)p.Q : (const void*)p.dO; }
   __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
-  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
+  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head, bool) {
     load_tile2(&p.mK64, nullptr, st, DC, ACH, BLK, bar, t * T, head);
   }
+  __device__ static void fill_vec(const Params&, float*, int, int, int) {}
   __device__ static void load_b(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
     load_tile2(&p.mV64, nullptr, st, DC, BCH, BLK, bar, t * T, head);
   }
@@ -282,11 +287,12 @@ struct PassZ {
     float nL, Di, alpha, ex;
   };
   __device__ static void ew_init(Row& w, const Params& p, int blk0, int r, int head) {
-    const size_t vo = (size_t)head * p.N + blk0 + r;
-    w.nL = -p.L[vo] * kLog2e;
-    w.Di = p.D[vo];
-    w.alpha = p.ws[2 * vo];                              // row totals of the U1 sweep
-    w.ex = fmaf(-w.Di, w.alpha, p.ws[2 * vo + 1]);       // EX = E - D alpha
+    const bool ok = blk0 + r < p.N;   // ragged N: rows past the end are never stored
+    const size_t vo = (size_t)head * p.N + (ok ? blk0 + r : 0);
+    w.nL = ok ? -p.L[vo] * kLog2e : 0.f;
+    w.Di = ok ? p.D[vo] : 0.f;
+    w.alpha = ok ? p.ws[2 * vo] : 0.f;                            // row totals of the U1 sweep
+    w.ex = ok ? fmaf(-w.Di, w.alpha, p.ws[2 * vo + 1]) : 0.f;     // EX = E - D alpha
   }
   template <bool MASK>
   __device__ static bool ew_tile(Row& w, const Params& p, const TileArgs& a, const TileSync& s, int r) {
@@ -320,12 +326,15 @@ struct PassZ {
     return true;
   }
   __device__ static void epilogue(Row&, const Params& p, const EpiArgs& e) {
-    const size_t ro = ((size_t)e.head * p.N + e.blk0 + e.r) * D;
+    // every lane runs the (warp-collective) TMEM loads; rows >= N touch no memory
+    const bool keep = e.blk0 + e.r < p.N;
+    const size_t ro = ((size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0)) * D;
     const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
 #pragma unroll 1
     for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
       float z[16], o[16];
       tmem_ld16(e.tm + c0, z);
+      if (!keep) continue;
       const float4* u1 = reinterpret_cast<const float4*>(p.gQ + ro + c0);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -353,7 +362,7 @@ struct PassY {
   static constexpr int SA = DC * ACH, SB = DC * BCH, SA_TX = SA, SB_TX = SB;
   static constexpr int NSA = 6, NSB = NSA;
   static constexpr bool VEC = false, ROW_SUMS = true, TS = true;
-  static constexpr int VEC_OFF = 0, OPS = 0;
+  static constexpr int VEC_OFF = 0, OPS = 0, NVEC = 0, VEC_SCRATCH = 0;
   static constexpr int ACC = D, SCOLS = 2 * T, NBUF = 2;   // [S | B]
   static constexpr int OP_HALF = T;                     // P, PB (32 columns each)
   static constexpr int OP_COL = ACC + NBUF * SCOLS;
@@ -364,9 +373,10 @@ struct PassY {
 
   __device__ static const void* tres_src(const Params& p, int s) { return s == 0 ? (const void*)p.Q : (const void*)p.UQ; }
   __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
-  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
+  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head, bool) {
     load_tile2(T == 64 ? &p.mV64 : &p.mV, T == 64 ? &p.mUV64 : &p.mUV, st, DC, ACH, BLK, bar, t * T, head);
   }
+  __device__ static void fill_vec(const Params&, float*, int, int, int) {}
   __device__ static void load_b(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
     load_tile2(T == 64 ? &p.mK64 : &p.mK, T == 64 ? &p.mUK64 : &p.mUK, st, DC, BCH, BLK, bar, t * T, head);
   }
@@ -393,7 +403,7 @@ struct PassY {
     float nL, alpha;
   };
   __device__ static void ew_init(Row& w, const Params& p, int blk0, int r, int head) {
-    w.nL = -p.L[(size_t)head * p.N + blk0 + r] * kLog2e;
+    w.nL = blk0 + r < p.N ? -p.L[(size_t)head * p.N + blk0 + r] * kLog2e : 0.f;
     w.alpha = 0.f;
   }
   template <bool MASK>
@@ -429,12 +439,15 @@ struct PassY {
   __device__ static void epilogue(Row& w, const Params& p, const EpiArgs& e) {
     float alpha = w.alpha, unused = 0.f;
     if (!e.sum_rows(alpha, unused)) return;
-    const size_t ro = ((size_t)e.head * p.N + e.blk0 + e.r) * D;
+    // every lane runs the (warp-collective) TMEM loads; rows >= N touch no memory
+    const bool keep = e.blk0 + e.r < p.N;
+    const size_t ro = ((size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0)) * D;
     const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
 #pragma unroll 1
     for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
       float y[16], o[16];
       tmem_ld16(e.tm + c0, y);
+      if (!keep) continue;
       const float4* src = reinterpret_cast<const float4*>(p.O + ro + c0);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -473,7 +486,9 @@ struct Pass2 {
   static constexpr int OP_HALF = 48;              // TMEM operands: dS, Gs, Gdp (16 columns each)
   static constexpr int OP_COL = ACC + NBUF * SCOLS;
   static constexpr int TRES_COL = OP_COL + (kAllTmem ? 2 * OP_HALF : 0);
-  static constexpr int SMEM = RES + NSA * SA + OPS;
+  static constexpr int NVEC = 4;                   // L, D, (alpha, E) per query
+  static constexpr int VEC_SCRATCH = RES + NSA * SA + OPS;   // 2 warpgroups x 2 buffers x NVEC x T floats
+  static constexpr int SMEM = VEC_SCRATCH + 4 * NVEC * T * 4;
   static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
   static_assert(SMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
   static constexpr int A_K = 0, A_V = D;
@@ -486,13 +501,14 @@ struct Pass2 {
     for (int s = 0; s < 2; ++s)
       for (int kc = 0; kc < DC; ++kc) tma_load_3d(res + (s * DC + kc) * kChunk, m[s], bar, kc * 64, col0, head);
   }
-  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
+  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head, bool whole) {
     for (int kc = 0; kc < DC; ++kc) {
       uint8_t* c = st + kc * ACH;
       tma_load_3d(c, &p.mQ, bar, kc * 64, t * kT, head);
       tma_load_3d(c + kBlk, &p.mUQ, bar, kc * 64, t * kT, head);
       tma_load_3d(c + 2 * kBlk, &p.mdO, bar, kc * 64, t * kT, head);
     }
+    if (!whole) return;   // ragged last tile: fill_vec
     const size_t v = (size_t)head * p.N + (size_t)t * kT;
     uint8_t* vec = st + VEC_OFF;
     bulk_load(vec, p.L + v, 128, bar);
@@ -500,6 +516,20 @@ struct Pass2 {
     bulk_load(vec + 256, p.ws + 2 * v, 256, bar);
   }
   __device__ static void load_b(const Params&, uint8_t*, uint64_t*, int, int) {}
+  // L, D, (alpha, E) of tile t with bounds checks (128 threads, thread i)
+  __device__ static void fill_vec(const Params& p, float* dst, int t, int head, int i) {
+    for (int k = i; k < 4 * T; k += 128) {
+      float v = 0.f;
+      if (k < 2 * T) {
+        const int q = t * T + (k % T);
+        if (q < p.N) v = (k < T ? p.L : p.D)[(size_t)head * p.N + q];
+      } else {
+        const int q = t * T + (k - 2 * T) / 2;
+        if (q < p.N) v = p.ws[2 * ((size_t)head * p.N + q) + (k & 1)];
+      }
+      dst[k] = v;
+    }
+  }
 
   __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t res, uint32_t sa, uint32_t) {
     const uint32_t i64 = idesc_bf16(kM, 64, false, false), i32 = idesc_bf16(kM, 32, false, false);
@@ -603,7 +633,9 @@ struct Pass2 {
   }
 
   __device__ static void epilogue(Row&, const Params& p, const EpiArgs& e) {
-    const size_t ro = ((size_t)e.head * p.N + e.blk0 + e.r) * D;
+    // every lane runs the (warp-collective) TMEM loads; rows >= N store nothing
+    const bool keep = e.blk0 + e.r < p.N;
+    const size_t ro = ((size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0)) * D;
     const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
 #pragma unroll 1
     for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
@@ -611,8 +643,10 @@ struct Pass2 {
       tmem_ld16x2(e.tm + A_K + c0, e.tm + A_V + c0, ak, av);
 #pragma unroll
       for (int j = 0; j < 16; ++j) ak[j] *= p.tau;
-      store16(p.gK + ro + c0, ak);
-      store16(p.gV + ro + c0, av);
+      if (keep) {
+        store16(p.gK + ro + c0, ak);
+        store16(p.gV + ro + c0, av);
+      }
     }
   }
 };
@@ -622,7 +656,10 @@ struct Pass2 {
 // ===========================================================================
 template <class Op>
 cudaError_t launch(const char* name, const typename Op::Params& prm, dim3 grid, cudaStream_t s) {
-  auto kernel = prm.causal ? tile_kernel<Op, true> : tile_kernel<Op, false>;
+  // the instantiation for (causal, ragged N)
+  const bool ragged = prm.N % kM != 0;
+  auto kernel = prm.causal ? (ragged ? tile_kernel<Op, true, true> : tile_kernel<Op, true, false>)
+                           : (ragged ? tile_kernel<Op, false, true> : tile_kernel<Op, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Op::SMEM);
   if (e != cudaSuccess) return e;
   prof_begin(s, name);
@@ -656,7 +693,7 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   p1.err = c.err;
   p1.wait_ns = c.wait_ns;
   p1.stall = c.stall;
-  const dim3 grid(N / kM, BH);
+  const dim3 grid((N + kM - 1) / kM, BH);
   // the Z kernel reads what the U1 kernel wrote (U1 in gQ, alpha and E)
   cudaError_t e = launch<PassU1<D>>("bob_pass1_u1", p1, grid, s);
   if (e == cudaSuccess) e = launch<PassZ<D>>("bob_pass1_z", p1, grid, s);

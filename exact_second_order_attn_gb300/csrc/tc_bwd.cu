@@ -1,5 +1,5 @@
 // Tensor-core (tcgen05 + TMEM + TMA) first backward for bf16 inputs, d in
-// {64, 128}, N a multiple of 128, on the tile skeleton of tc_tile.cuh.  It
+// {64, 128}, any N, on the tile skeleton of tc_tile.cuh.  It
 // produces dQ, dK, dV and D = rowsum(dO o O), the row term BoB reads.
 //
 // Source: "FlashBoB: I/O-Efficient Exact Backward-over-Backward for Softmax
@@ -55,7 +55,7 @@ struct DqOp {
   static constexpr int SA = DC * ACH, SB = DC * BCH, SA_TX = SA, SB_TX = SB;
   static constexpr int NSA = D == 128 ? 5 : 8, NSB = NSA;
   static constexpr bool VEC = false, ROW_SUMS = false, TS = D == 64;
-  static constexpr int VEC_OFF = 0;
+  static constexpr int VEC_OFF = 0, NVEC = 0, VEC_SCRATCH = 0;
   static constexpr int OPS = TS ? 0 : 2 * tile::kChunk;  // dS, one [128][64] tile per half
   static constexpr int ACC = D, SCOLS = 2 * T, NBUF = 2;   // [S | dP]
   static constexpr int OP_HALF = T / 2, OP_COL = ACC + NBUF * SCOLS;
@@ -66,9 +66,10 @@ struct DqOp {
 
   __device__ static const void* tres_src(const Params& p, int s) { return s == 0 ? (const void*)p.Q : (const void*)p.dO; }
   __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
-  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
+  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head, bool) {
     for (int kc = 0; kc < DC; ++kc) tma_load_3d(st + kc * ACH, &p.mK, bar, kc * 64, t * T, head);
   }
+  __device__ static void fill_vec(const Params&, float*, int, int, int) {}
   __device__ static void load_b(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
     for (int kc = 0; kc < DC; ++kc) tma_load_3d(st + kc * BCH, &p.mV, bar, kc * 64, t * T, head);
   }
@@ -96,6 +97,9 @@ struct DqOp {
     float nL, Di;
   };
   __device__ static void ew_init(Row& w, const Params& p, int blk0, int r, int head) {
+    w.Di = 0.f;
+    w.nL = 0.f;
+    if (blk0 + r >= p.N) return;   // ragged N: row past the end (never stored)
     const size_t vo = (size_t)head * p.N + blk0 + r;
     const size_t ro = vo * D;
     // D_i = rowsum(dO o O) of this thread's row
@@ -150,7 +154,9 @@ struct DqOp {
     return true;
   }
   __device__ static void epilogue(Row&, const Params& p, const tile::EpiArgs& e) {
-    const size_t ro = ((size_t)e.head * p.N + e.blk0 + e.r) * D;
+    // every lane runs the (warp-collective) TMEM loads; rows >= N store nothing
+    const bool keep = e.blk0 + e.r < p.N;
+    const size_t ro = ((size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0)) * D;
     const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
 #pragma unroll 1
     for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
@@ -158,7 +164,7 @@ struct DqOp {
       tmem_ld16(e.tm + c0, v);
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] *= p.tau;
-      tile::store16(p.dQ + ro + c0, v);
+      if (keep) tile::store16(p.dQ + ro + c0, v);
     }
   }
 };
@@ -193,20 +199,31 @@ struct DkvOp {
   static constexpr int ACC = 2 * D, SCOLS = 2 * T, NBUF = D == 128 ? 1 : 2;   // dK, dV; [S^T | dP^T]
   static constexpr int OP_HALF = 0, OP_COL = ACC + NBUF * SCOLS;
   static constexpr int TRES_COL = OP_COL;
-  static constexpr int SMEM = NSA * SA + OPS;
+  static constexpr int NVEC = 2;                          // L, D per query
+  static constexpr int VEC_SCRATCH = NSA * SA + OPS;      // 2 warpgroups x 2 buffers x NVEC x T floats
+  static constexpr int SMEM = VEC_SCRATCH + 4 * NVEC * T * 4;
   static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
   static_assert(SMEM + 1024 <= 232448, "shared memory budget");
 
   __device__ static const void* tres_src(const Params& p, int s) { return s == 0 ? (const void*)p.K : (const void*)p.V; }
   __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
-  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
+  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head, bool whole) {
     for (int kc = 0; kc < DC; ++kc) {
       tma_load_3d(st + kc * ACH, &p.mQ, bar, kc * 64, t * T, head);
       tma_load_3d(st + kc * ACH + BLK, &p.mdO, bar, kc * 64, t * T, head);
     }
+    if (!whole) return;   // ragged last tile: fill_vec
     const size_t v = (size_t)head * p.N + (size_t)t * T;
     tile::bulk_load(st + VEC_OFF, p.L + v, T * 4, bar);
     tile::bulk_load(st + VEC_OFF + T * 4, p.D + v, T * 4, bar);
+  }
+  // L, D of tile t with bounds checks (128 threads, thread i)
+  __device__ static void fill_vec(const Params& p, float* dst, int t, int head, int i) {
+    for (int k = i; k < 2 * T; k += 128) {
+      const int q = t * T + (k % T);
+      const float* src = k < T ? p.L : p.D;
+      dst[k] = q < p.N ? src[(size_t)head * p.N + q] : 0.f;
+    }
   }
   __device__ static void load_b(const Params&, uint8_t*, uint64_t*, int, int) {}
   __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t, uint32_t sa, uint32_t) {
@@ -274,7 +291,9 @@ struct DkvOp {
     return true;
   }
   __device__ static void epilogue(Row&, const Params& p, const tile::EpiArgs& e) {
-    const size_t ro = ((size_t)e.head * p.N + e.blk0 + e.r) * D;
+    // every lane runs the (warp-collective) TMEM loads; rows >= N store nothing
+    const bool keep = e.blk0 + e.r < p.N;
+    const size_t ro = ((size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0)) * D;
     const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
 #pragma unroll 1
     for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
@@ -282,8 +301,10 @@ struct DkvOp {
       tmem_ld16x2(e.tm + c0, e.tm + D + c0, k_, v);
 #pragma unroll
       for (int j = 0; j < 16; ++j) k_[j] *= p.tau;
-      tile::store16(p.dK + ro + c0, k_);
-      tile::store16(p.dV + ro + c0, v);
+      if (keep) {
+        tile::store16(p.dK + ro + c0, k_);
+        tile::store16(p.dV + ro + c0, v);
+      }
     }
   }
 };
@@ -299,6 +320,13 @@ cudaError_t launch(const char* name, K kernel, int smem, int threads, dim3 grid,
   kernel<<<grid, threads, smem, s>>>(prm);
   prof_end(s);
   return cudaGetLastError();
+}
+
+// the instantiation for (causal, ragged N)
+template <class Op>
+auto pick(bool causal, bool ragged) {
+  return causal ? (ragged ? tile::tile_kernel<Op, true, true> : tile::tile_kernel<Op, true, false>)
+                : (ragged ? tile::tile_kernel<Op, false, true> : tile::tile_kernel<Op, false, false>);
 }
 
 template <int D>
@@ -318,9 +346,9 @@ cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
   q.err = c.err;
   q.wait_ns = c.wait_ns;
   q.stall = c.stall;
-  const dim3 grid(a.N / kM, a.BH);
-  cudaError_t e = launch("attn_bwd_dq", a.causal ? tile::tile_kernel<DqOp<D>, true> : tile::tile_kernel<DqOp<D>, false>,
-                         DqOp<D>::SMEM, tile::kThreads, grid, q, s);
+  const dim3 grid((a.N + kM - 1) / kM, a.BH);
+  const bool ragged = a.N % kM != 0;
+  cudaError_t e = launch("attn_bwd_dq", pick<DqOp<D>>(a.causal, ragged), DqOp<D>::SMEM, tile::kThreads, grid, q, s);
   if (e != cudaSuccess) return e;
   DkvParams k;
   if (!make_bf16_map(&k.mQ, a.Q, a.BH, a.N, D, DkvOp<D>::T) || !make_bf16_map(&k.mdO, a.dO, a.BH, a.N, D, DkvOp<D>::T))
@@ -337,8 +365,7 @@ cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
   k.err = c.err;
   k.wait_ns = c.wait_ns;
   k.stall = c.stall;
-  return launch("attn_bwd_dkdv", a.causal ? tile::tile_kernel<DkvOp<D>, true> : tile::tile_kernel<DkvOp<D>, false>,
-                DkvOp<D>::SMEM, tile::kThreads, grid, k, s);
+  return launch("attn_bwd_dkdv", pick<DkvOp<D>>(a.causal, ragged), DkvOp<D>::SMEM, tile::kThreads, grid, k, s);
 }
 
 }  // namespace

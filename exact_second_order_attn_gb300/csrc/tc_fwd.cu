@@ -1,5 +1,5 @@
 // Tensor-core (tcgen05 + TMEM + TMA) attention forward for bf16 inputs,
-// d in {64, 128}, N a multiple of 128: O = softmax(tau Q K^T) V and the
+// d in {64, 128}, any N: O = softmax(tau Q K^T) V and the
 // natural-log row logsumexp L (FlashBoB abstract: the FlashAttention-style
 // forward whose outputs the first backward and BoB consume).
 //
@@ -94,7 +94,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t s_col, uint32_t o_col, int
     if (t > 0) {
       const float scale = tile::ex2(m - mn);
       // the previous P V product of this block must have landed
-      if (!mbar_wait(&o_done, (t - 1) & 1, wt)) return false;
+      if (!__all_sync(0xffffffffu, mbar_wait(&o_done, (t - 1) & 1, wt))) return false;
       tc_fence_after();
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 16) {
@@ -127,7 +127,10 @@ __device__ __forceinline__ bool softmax_tile(uint32_t s_col, uint32_t o_col, int
   return true;
 }
 
-template <int D, bool CAUSAL>
+// CAUSAL and RAGGED (N not a multiple of 128) are compile-time choices; a
+// ragged N reads zeros past the end (TMA), masks keys >= N in the last tile
+// and stores only rows < N.
+template <int D, bool CAUSAL, bool RAGGED>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -137,8 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc(const __grid_constant
   // row0 / 128 + X), so the last pairs of blocks do the most work and run first
   const int pair = CAUSAL ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
   const int row0 = pair * 2 * kM, head = blockIdx.y;
-  const int nblk = (row0 + kM < p.N) ? 2 : 1;   // block B exists unless N is an odd multiple of 128
-  const int ntx[2] = {CAUSAL ? row0 / kKT + 1 : p.N / kKT, CAUSAL ? row0 / kKT + 2 : p.N / kKT};
+  const int nblk = (row0 + kM < p.N) ? 2 : 1;   // block B exists unless it would start at or past N
+  const int t_all = (p.N + kKT - 1) / kKT;
+  const int ntx[2] = {CAUSAL ? min(t_all, row0 / kKT + 1) : t_all, CAUSAL ? min(t_all, row0 / kKT + 2) : t_all};
   const int nt = ntx[nblk - 1];                 // key tiles the CTA streams
 
   if (tid == 0) {
@@ -275,14 +279,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc(const __grid_constant
     bool ok = live && x < nblk;
     const int ntb = ntx[x < nblk ? x : 0];
     for (int t = 0; t < ntb && ok; ++t) {
-      if (!mbar_wait(&ctrl.s_full[x], t & 1, wt)) { ok = false; break; }
+      // warp-uniform waits: the TMEM loads and stores that follow are warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(&ctrl.s_full[x], t & 1, wt))) { ok = false; break; }
       tc_fence_after();
       // this row may see tile columns 0..lim (causal: keys up to its own index);
       // the masked variant runs only on a block's diagonal tile
-      const int lim = CAUSAL ? row0 + x * kM + r - t * kKT : kKT - 1;
+      int lim = CAUSAL ? row0 + x * kM + r - t * kKT : kKT - 1;
+      if (RAGGED) lim = min(lim, p.N - 1 - t * kKT);   // keys >= N
       float ls = 0.f;
-      const bool fine = (CAUSAL && __any_sync(0xffffffffu, lim < kKT - 1))
-                            ? softmax_tile<D, CAUSAL>(s_col, tb + lane + x * D, lim, sc, m, l, ls, ctrl.o_done[x], t, wt)
+      const bool fine = ((CAUSAL || RAGGED) && __any_sync(0xffffffffu, lim < kKT - 1))
+                            ? softmax_tile<D, CAUSAL || RAGGED>(s_col, tb + lane + x * D, lim, sc, m, l, ls, ctrl.o_done[x], t, wt)
                             : softmax_tile<D, false>(s_col, tb + lane + x * D, lim, sc, m, l, ls, ctrl.o_done[x], t, wt);
       if (!fine) { ok = false; break; }
       l += ls;
@@ -290,10 +296,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc(const __grid_constant
       tc_fence_before();
       mbar_arrive(&ctrl.p_full[x]);
     }
-    if (ok && mbar_wait(&ctrl.o_done[x], (ntb - 1) & 1, wt)) {
+    if (ok && __all_sync(0xffffffffu, mbar_wait(&ctrl.o_done[x], (ntb - 1) & 1, wt))) {
       tc_fence_after();
+      // every lane runs the (warp-collective) TMEM loads; rows >= N store nothing
       const int i = row0 + x * kM + r;
-      const size_t ro = ((size_t)head * p.N + i) * D;
+      const bool keep = i < p.N;
+      const size_t ro = ((size_t)head * p.N + (keep ? i : 0)) * D;
       const float inv = 1.f / l;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 16) {
@@ -301,9 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc(const __grid_constant
         tmem_ld16(tb + lane + x * D + c0, o);
 #pragma unroll
         for (int e = 0; e < 16; ++e) o[e] *= inv;
-        tile::store16(p.O + ro + c0, o);
+        if (keep) tile::store16(p.O + ro + c0, o);
       }
-      p.L[(size_t)head * p.N + i] = (m + __log2f(l)) * kLn2;
+      if (keep) p.L[(size_t)head * p.N + i] = (m + __log2f(l)) * kLn2;
     }
   }
   tc_fence_before();
@@ -328,7 +336,9 @@ cudaError_t fwd_d(const FwdArgs& a, const DevCtx& c, cudaStream_t s) {
   p.err = c.err;
   p.wait_ns = c.wait_ns;
   p.stall = c.stall;
-  auto kernel = a.causal ? attn_fwd_tc<D, true> : attn_fwd_tc<D, false>;
+  const bool ragged = a.N % kM != 0;
+  auto kernel = a.causal ? (ragged ? attn_fwd_tc<D, true, true> : attn_fwd_tc<D, true, false>)
+                         : (ragged ? attn_fwd_tc<D, false, true> : attn_fwd_tc<D, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((a.N + 2 * kM - 1) / (2 * kM), a.BH);

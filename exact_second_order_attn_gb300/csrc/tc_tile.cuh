@@ -104,6 +104,7 @@ struct Ctrl {
   uint64_t o_full[2], o_empty[2];
   uint64_t acc_full, drain, drain_acc;
   uint64_t red;          // epilogue: both warpgroups' row partials written
+  uint64_t vfill[2];     // ragged N: a warpgroup's vectors written to its scratch
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -133,8 +134,9 @@ struct TileSync {
   }
   // wait until the accumulator MMAs of this group's previous tile have read
   // the operand half
+  // (warp-uniform: the TMEM stores that follow are warp-collective)
   __device__ __forceinline__ bool acquire_ops() const {
-    return mbar_wait(&c->o_empty[q], (k & 1) ^ 1, *w);
+    return __all_sync(0xffffffffu, mbar_wait(&c->o_empty[q], (k & 1) ^ 1, *w));
   }
   // operands written: hand them to the MMA thread (and release the ring-A
   // vectors this warpgroup read)
@@ -168,7 +170,8 @@ struct EpiArgs {
     float2* red = reinterpret_cast<float2*>(scratch);
     red[g * 128 + r] = make_float2(a, b);
     mbar_arrive(&c->red);
-    if (!mbar_wait(&c->red, 0, *w)) return false;
+    // warp-uniform: the caller's TMEM loads that follow are warp-collective
+    if (!__all_sync(0xffffffffu, mbar_wait(&c->red, 0, *w))) return false;
     const float2 x = red[r], y = red[128 + r];
     a = x.x + y.x;
     b = x.y + y.y;
@@ -187,9 +190,17 @@ struct TileArgs {
   int lo, hi;          // tile columns [lo, hi] this thread's row may see (causal mask; else [0, T-1])
 };
 
-// CAUSAL is a compile-time choice, so the full-attention kernels carry no
-// mask code; the host launches the instantiation that matches p.causal.
-template <class Op, bool CAUSAL>
+// CAUSAL and RAGGED (N not a multiple of 128) are compile-time choices, so
+// the kernels for full attention on whole tiles carry no mask code; the host
+// launches the instantiation that matches the problem.
+//
+// Ragged N: TMA fills rows at or beyond N with zeros; the streamed tile that
+// crosses N masks its columns >= N like the causal mask; resident rows >= N
+// are computed on zeros and never stored; per-tile vectors (column kernels)
+// of that last tile - of every tile when N is not a multiple of 4, since a
+// bulk copy needs a 16-byte aligned source and head h starts at float h N -
+// are read with bounds checks instead of a bulk copy.
+template <class Op, bool CAUSAL, bool RAGGED>
 __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant__ typename Op::Params p) {
   static_assert(Op::NSB == 0 || Op::NSB == Op::NSA, "ring B stages pair with ring A stages");
   static_assert(Op::NBUF < Op::NSA, "the MMA order needs more stages than score buffers");
@@ -204,8 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
   // diagonal.  Row blocks then run the heaviest (last) blocks first.
   const int blk = (Op::ROWS && CAUSAL) ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
   const int blk0 = blk * kM, head = blockIdx.y;
+  const int t_all = (p.N + Op::T - 1) / Op::T;
   const int t_begin = (CAUSAL && !Op::ROWS) ? blk0 / Op::T : 0;
-  const int t_end = (CAUSAL && Op::ROWS) ? (blk0 + kM) / Op::T : p.N / Op::T;
+  const int t_end = (CAUSAL && Op::ROWS) ? min(t_all, (blk0 + kM) / Op::T) : t_all;
   const int nt = t_end - t_begin;   // loop steps; step t streams tile t_begin + t
   uint8_t* res = smem;
   uint8_t* ring_a = res + Op::RES;
@@ -231,6 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
     mbar_init(&ctrl.drain, 1);
     mbar_init(&ctrl.drain_acc, 1);
     mbar_init(&ctrl.red, 256);
+    mbar_init(&ctrl.vfill[0], 128);
+    mbar_init(&ctrl.vfill[1], 128);
     fence_mbar_init();
     if ((smem_u32(smem) & 1023u) != 0u) {  // layout assumption; never expected
       ctrl.abort_flag = 1;
@@ -271,8 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
           if (!(ok = mbar_wait(&ctrl.b_empty[sa], ((t / Op::NSA) & 1) ^ 1, wt))) break;
         }
         if (p.stall && t == 0) continue;  // test hook: nothing will fill this stage
-        mbar_arrive_expect_tx(&ctrl.a_full[sa], Op::SA_TX + (Op::NSB > 0 ? Op::SB_TX : 0));
-        Op::load_a(p, ring_a + sa * Op::SA, &ctrl.a_full[sa], t_begin + t, head);
+        // vectors by bulk copy only for whole tiles at 16-byte aligned addresses
+        const bool whole = !RAGGED || (p.N % 4 == 0 && (t_begin + t + 1) * Op::T <= p.N);
+        mbar_arrive_expect_tx(&ctrl.a_full[sa],
+                              Op::SA_TX + (Op::NSB > 0 ? Op::SB_TX : 0) - (Op::VEC && !whole ? 4 * Op::T * Op::NVEC : 0));
+        Op::load_a(p, ring_a + sa * Op::SA, &ctrl.a_full[sa], t_begin + t, head, whole);
         if constexpr (Op::NSB > 0) Op::load_b(p, ring_b + sa * Op::SB, &ctrl.a_full[sa], t_begin + t, head);
         FBOB_STAMP(7, t);
         ia = t + 1;
@@ -358,7 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
     typename Op::Row row;
     if constexpr (Op::TRES > 0) {
       // resident rows -> TMEM: warpgroup g copies residents g, g + 2, ...
-      const size_t row_g = (size_t)head * p.N + blk0 + r;
+      // (rows at or beyond N are zeros)
+      const bool row_ok = blk0 + r < p.N;
+      const size_t row_g = (size_t)head * p.N + (row_ok ? blk0 + r : 0);
       for (int s = g; s < Op::TRES; s += 2) {
         const uint4* src = reinterpret_cast<const uint4*>(Op::tres_src(p, s)) + row_g * (Op::D / 8);
         const uint32_t col = tb + lane + Op::TRES_COL + (uint32_t)(s * (Op::D / 2));
@@ -367,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
           uint32_t w[16];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const uint4 u = src[4 * c + q];
+            const uint4 u = row_ok ? src[4 * c + q] : make_uint4(0u, 0u, 0u, 0u);
             w[4 * q] = u.x;
             w[4 * q + 1] = u.y;
             w[4 * q + 2] = u.z;
@@ -382,11 +401,14 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
     }
     Op::ew_init(row, p, blk0, r, head);
     bool ok = live;
+    int nfill = 0;   // uses of this warpgroup's vector scratch (double-buffered)
     for (int t = kSplit ? 0 : g; t < nt && ok; t += kSplit ? 1 : 2) {
       const int q = t & 1, k = t >> 1, sa = t % Op::NSA;
       FBOB_STAMP(8, t);
-      if (Op::VEC && !mbar_wait(&ctrl.a_full[sa], (t / Op::NSA) & 1, wt)) { ok = false; break; }
-      if (!mbar_wait(&ctrl.s_full[q], k & 1, wt)) { ok = false; break; }
+      // waits are warp-uniform: a warp must never split in front of the
+      // warp-collective TMEM loads and stores of the tile
+      if (Op::VEC && !__all_sync(0xffffffffu, mbar_wait(&ctrl.a_full[sa], (t / Op::NSA) & 1, wt))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(&ctrl.s_full[q], k & 1, wt))) { ok = false; break; }
       FBOB_STAMP(2, t);
       tc_fence_after();
 #ifdef FBOB_TRACE
@@ -397,6 +419,18 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
       TileArgs ta;
       ta.sc = tb + lane + Op::ACC + (t % Op::NBUF) * Op::SCOLS;
       ta.vec = Op::VEC ? reinterpret_cast<const float*>(ring_a + sa * Op::SA + Op::VEC_OFF) : nullptr;
+      if (Op::VEC && RAGGED && (p.N % 4 != 0 || (t_begin + t + 1) * Op::T > p.N)) {
+        // no bulk copy for this tile (see the producer): the warpgroup reads
+        // the tile's vectors itself
+        // buffer nfill % 2: its previous reader finished before this
+        // warpgroup's previous rendezvous, which every thread has passed
+        float* scr = reinterpret_cast<float*>(smem + Op::VEC_SCRATCH) + (2 * g + (nfill & 1)) * (Op::NVEC * Op::T);
+        Op::fill_vec(p, scr, t_begin + t, head, r);
+        mbar_arrive(&ctrl.vfill[g]);   // bounded rendezvous of the warpgroup
+        if (!__all_sync(0xffffffffu, mbar_wait(&ctrl.vfill[g], nfill & 1, wt))) { ok = false; break; }
+        ++nfill;
+        ta.vec = scr;
+      }
       ta.ops = Op::TS ? (tb + lane + Op::OP_COL + (uint32_t)q * Op::OP_HALF) : smem_u32(ops);
       ta.h = (uint32_t)q;
       ta.t = t_begin + t;
@@ -405,17 +439,19 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
       const int diag = blk0 + r - ta.t * Op::T;   // this row's own index, as a tile column
       ta.lo = (CAUSAL && !Op::ROWS) ? diag : 0;
       ta.hi = (CAUSAL && Op::ROWS) ? diag : Op::T - 1;
+      if (RAGGED) ta.hi = min(ta.hi, p.N - 1 - ta.t * Op::T);   // columns >= N
       // tiles that cross the diagonal (causal) take the masked variant; the
       // vote keeps the choice warp-uniform
-      if (CAUSAL && __any_sync(0xffffffffu, ta.lo > 0 || ta.hi < Op::T - 1))
-        ok = Op::template ew_tile<CAUSAL>(row, p, ta, sync, r);
+      constexpr bool kMask = CAUSAL || RAGGED;
+      if (kMask && __any_sync(0xffffffffu, ta.lo > 0 || ta.hi < Op::T - 1))
+        ok = Op::template ew_tile<kMask>(row, p, ta, sync, r);
       else
         ok = Op::template ew_tile<false>(row, p, ta, sync, r);
       FBOB_STAMP(6, t);
 
     }
     const EpiArgs ea{tb + lane, reinterpret_cast<float*>(ring_a), &ctrl, &wt, blk0, r, head, g};
-    if (ok && mbar_wait(&ctrl.acc_full, 0, wt)) {
+    if (ok && __all_sync(0xffffffffu, mbar_wait(&ctrl.acc_full, 0, wt))) {
       tc_fence_after();
       Op::epilogue(row, p, ea);
     } else if (Op::ROW_SUMS) {

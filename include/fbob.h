@@ -32,8 +32,8 @@
  *   fp32.
  * - Every pointer must be 16-byte aligned and tensors must not overlap an
  *   output of the same call.
- * - Supported: d in {64, 128}; any N >= 1 for fp32 inputs; N a multiple of
- *   128 for bf16 inputs; causal or not.  B*H*N == 0 is a valid empty problem
+ * - Supported: d in {64, 128}; any N >= 1 (bf16 and fp32); causal or not.
+ *   B*H*N == 0 is a valid empty problem
  *   (returns FBOB_OK, launches nothing).
  * - Argument problems are reported BEFORE any launch (nothing is launched on
  *   error).  A failed launch returns FBOB_ERR_CUDA.  Kernels never trap: a

@@ -79,7 +79,6 @@ def call_bob(lib, p, ptrs=None, ws=0x10000, ws_bytes=None):
     ("dtype", 7, _lib.ERR_INVALID_ARG),
     ("tau", float("nan"), _lib.ERR_INVALID_ARG),
     ("tau", 0.0, _lib.ERR_INVALID_ARG),
-    ("N", 200, _lib.ERR_UNSUPPORTED),          # bf16 needs N % 128 == 0
 ])
 def test_bad_problem_rejected_before_launch(lib, field, value, status):
     p = _lib.Problem(1, 2, 256, 64, 0.125, _lib.BF16, 0)
@@ -120,11 +119,12 @@ def test_causal_passes_validation(lib):
         assert call_bob(lib, p) in (_lib.OK, _lib.ERR_CUDA)
 
 
-def test_fp32_allows_ragged_n_at_validation(lib):
-    # validation passes; without a GPU the first CUDA call then fails cleanly
-    p = _lib.Problem(1, 1, 200, 64, 0.125, _lib.FP32, 0)
-    s = call_bob(lib, p)
-    assert s in (_lib.OK, _lib.ERR_CUDA)
+def test_ragged_n_passes_validation(lib):
+    # any N >= 1 for both dtypes; without a GPU the first CUDA call then fails cleanly
+    for dt in (_lib.BF16, _lib.FP32):
+        for N in (1, 200, 129):
+            p = _lib.Problem(1, 1, N, 64, 0.125, dt, 0)
+            assert call_bob(lib, p) in (_lib.OK, _lib.ERR_CUDA)
 
 
 def test_wait_limit_roundtrip(lib):
