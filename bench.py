@@ -139,15 +139,17 @@ def run_ours(args, w):
     L, D = torch.empty(shp[:3], **f32), torch.empty(shp[:3], **f32)
     wsp = torch.empty(shp[:3] + (2,), **f32)
 
+    cz = dict(causal=args.causal)
+
     def step():
-        fb.attn_fwd(x["Q"], x["K"], x["V"], w.tau, O, L)
-        fb.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], L, w.tau, dQ, dK, dV, D)
+        fb.attn_fwd(x["Q"], x["K"], x["V"], w.tau, O, L, **cz)
+        fb.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], L, w.tau, dQ, dK, dV, D, **cz)
         fb.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], L, D, x["UQ"], x["UK"], x["UV"], w.tau,
-                    gQ, gK, gV, gdO, wsp)
+                    gQ, gK, gV, gdO, wsp, **cz)
 
     def bob_only():
         fb.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], L, D, x["UQ"], x["UK"], x["UV"], w.tau,
-                    gQ, gK, gV, gdO, wsp)
+                    gQ, gK, gV, gdO, wsp, **cz)
 
     def barrier():
         if ws > 1:
@@ -215,13 +217,14 @@ def run_ours(args, w):
     fb.device_status()
 
     heads = w.B * w.H
-    unit = w.N * w.N * w.d * heads
+    # causal: every GEMM covers the N (N + 1) / 2 unmasked (query, key) pairs
+    pairs = causal_fraction(w.N) if args.causal else 1.0
+    unit = w.N * w.N * w.d * heads * pairs
     flops_step = (FLOPS_FWD + FLOPS_BWD + FLOPS_BOB) * unit
     flops_bob = FLOPS_BOB * unit
     hbm, pk, pk_sus, pk_kind = peaks()
     value = job_tflops(ws, flops_step, step_ms)
     bob_tf = flops_bob / (bob_ms * 1e-3) / 1e12
-    launches_per_step = 1 + 2 + (3 if w.d == 128 else 2)  # fwd, bwd (2), BoB (2 or 3)
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws,
@@ -229,8 +232,11 @@ def run_ours(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded iid Gaussian, bf16 inputs, fp32 accumulation and outputs)",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "tau": w.tau,
+                       "causal": bool(args.causal),
                        "step": "fwd + first bwd + BoB (pass 1 + pass 2)",
-                       "flops_per_step": flops_step, "flop_count": "52 N^2 d per head (fwd 4, bwd 10, BoB 38)",
+                       "flops_per_step": flops_step,
+                       "flop_count": "52 N^2 d per head (fwd 4, bwd 10, BoB 38)"
+                                     + (", times (N+1)/(2N) for the causal mask" if args.causal else ""),
                        "l2": "inputs (%.0f MB) larger than the 129 MB L2; no flush" % (h2d / 1e6),
                        "parallelism": f"replicas x{ws}"},
             "bob": {"ms_per_call": round(bob_ms, 4), "tflops": round(bob_tf, 3),
@@ -238,11 +244,12 @@ def run_ours(args, w):
                     "counted_flops": flops_bob},
             "e2e": {"value": round(job_tflops(ws, flops_step, e2e_ms), 3), "unit": "TFLOP/s",
                     "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step * args.steps,
+            # our kernels launched in the timed region (per-kernel records of the library)
+            "gpu_launches": int(sum(v[0] for v in kernels.values())),
             "clocks": clk,
         }
         line["kernels"] = {k: {"launches": v[0], "avg_ms": round(v[1] / v[0], 4)} for k, v in kernels.items()}
-        line["roofline"] = roofline(w, kernels, pk_sus)
+        line["roofline"] = roofline(w, kernels, pk_sus, pairs)
         line["cpu_baseline"] = cpu_baseline(w, args, head0(host))
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -294,7 +301,12 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def roofline(w, kernels, peak):
+def causal_fraction(N):
+    """Share of (query, key) pairs a causal mask keeps: N (N + 1) / 2 of N^2."""
+    return (N + 1) / (2.0 * N)
+
+
+def roofline(w, kernels, peak, pairs=1.0):
     """Roofline of the dominant kernel (largest share of the timed region):
     counted FLOPs per launch / its average launch time (CUDA events recorded by
     the library on the launching stream during the timed loop), against the
@@ -305,14 +317,15 @@ def roofline(w, kernels, peak):
         return None
     name, (n, total, _, _) = max(kernels.items(), key=lambda kv: kv[1][1])
     avg_ms = total / n
-    flops = COUNTED_GEMMS.get(name, 0) * 2 * w.N * w.N * w.d * w.B * w.H
+    flops = COUNTED_GEMMS.get(name, 0) * 2 * w.N * w.N * w.d * w.B * w.H * pairs
     achieved = flops / (avg_ms * 1e-3) / 1e12
     traffic = None
     try:
         with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
             rec = json.load(f)
         k = rec["kernels"].get(name)
-        if k and rec.get("source_hash") == kernel_source_hash() and k["d"] == w.d and k["N"] == w.N:
+        if (k and pairs == 1.0 and rec.get("source_hash") == kernel_source_hash() and k["d"] == w.d
+                and k["N"] == w.N):
             traffic = k["bytes_per_launch"] * (w.B * w.H) / k["heads"]
     except (OSError, KeyError, ValueError):
         traffic = None
@@ -326,17 +339,25 @@ def head0(inp):
     return {k: v[0, 0].double().numpy() for k, v in inp.items()}
 
 
-def oracle_sample(w, x, rows):
+def oracle_sample(w, x, rows, causal=False):
     """One bounded sample of the workload on the CPU oracle: query rows
     [0, rows) of head (0, 0) through forward, first backward and BoB (each
-    row block's work is exactly rows/N of the head's)."""
+    row block's work is exactly rows/N of the head's; with the causal mask
+    the sampled rows keep rows (rows + 1) / 2 (query, key) pairs)."""
+    import numpy as np
+
     import oracle.attention as orc
     r = slice(0, rows)
+    q = np.arange(rows) if causal else None
     t = time.perf_counter()
-    orc.attn_fwd_head(x["Q"][r], x["K"], x["V"], w.tau)
-    orc.attn_bwd_rows(x["Q"][r], x["K"], x["V"], x["dO"][r], w.tau)
-    orc.bob_rows(x["Q"][r], x["K"], x["V"], x["dO"][r], x["UQ"][r], x["UK"], x["UV"], w.tau)
+    orc.attn_fwd_head(x["Q"][r], x["K"], x["V"], w.tau, q)
+    orc.attn_bwd_rows(x["Q"][r], x["K"], x["V"], x["dO"][r], w.tau, q)
+    orc.bob_rows(x["Q"][r], x["K"], x["V"], x["dO"][r], x["UQ"][r], x["UK"], x["UV"], w.tau, q)
     return time.perf_counter() - t
+
+
+def sample_pairs(w, rows, causal):
+    return rows * (rows + 1) / 2 if causal else rows * w.N
 
 
 def blas_threads():
@@ -349,8 +370,8 @@ def blas_threads():
 
 def cpu_baseline(w, args, x):
     rows = args.baseline_rows
-    secs = oracle_sample(w, x, rows)
-    flops = (FLOPS_FWD + FLOPS_BWD + FLOPS_BOB) * rows * w.N * w.d
+    secs = oracle_sample(w, x, rows, args.causal)
+    flops = (FLOPS_FWD + FLOPS_BWD + FLOPS_BOB) * sample_pairs(w, rows, args.causal) * w.d
     return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(),
             "kind": "oracle", "seconds": round(secs, 3),
             "sample": f"query rows [0,{rows}) of head (0,0) of {w.name}: fwd + first bwd + BoB rows, "
@@ -364,10 +385,10 @@ def run_reference(args, w):
     import attn_inputs
     x = head0(attn_inputs.make_inputs(w))
     for _ in range(args.warmup):
-        oracle_sample(w, x, args.cpu_rows)
-    times = [oracle_sample(w, x, args.cpu_rows) for _ in range(args.steps)]
+        oracle_sample(w, x, args.cpu_rows, args.causal)
+    times = [oracle_sample(w, x, args.cpu_rows, args.causal) for _ in range(args.steps)]
     secs = statistics.mean(times)
-    flops = (FLOPS_FWD + FLOPS_BWD + FLOPS_BOB) * args.cpu_rows * w.N * w.d
+    flops = (FLOPS_FWD + FLOPS_BWD + FLOPS_BOB) * sample_pairs(w, args.cpu_rows, args.causal) * w.d
     value = flops / secs / 1e12
     cb = {"value": round(value, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
           "sample": f"query rows [0,{args.cpu_rows}) of head (0,0) of {w.name} per step"}
@@ -375,7 +396,7 @@ def run_reference(args, w):
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(secs * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": bool(args.causal),
                        "step": "fwd + first bwd + BoB on the sampled rows"},
             "cpu_baseline": cb,
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -394,6 +415,8 @@ def main():
                     help="query rows of one head per reference-arm step (CPU oracle)")
     ap.add_argument("--baseline-rows", type=int, default=8192,
                     help="query rows of one head in the cpu_baseline sample")
+    ap.add_argument("--causal", action="store_true",
+                    help="causal mask (query i attends to keys j <= i); counted FLOPs scale by (N+1)/(2N)")
     ap.add_argument("--once", action="store_true",
                     help="run --warmup + 1 steps and exit without timing (for profiler captures)")
     args = ap.parse_args()
