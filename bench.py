@@ -40,12 +40,12 @@ FLOPS_FWD, FLOPS_BWD, FLOPS_BOB = 4, 10, 38   # x N^2 d per head
 DEFAULT_WORKLOAD = "wide_head_b2h16_n16384_d128"
 # Counted GEMMs (2 N^2 d FLOPs each, per head) attributed to each kernel: the
 # 38 N^2 d of BoB = pass 1 (11: S, dP, C, B x2, U1 x2, U2, W, Y x2) + pass 2
-# (8).  Pass 1 runs as three sweeps: U1 (the five score GEMMs + U1 x2 = 7),
-# Z (one GEMM doing the work of U2 and W: 2) and Y (2); the recomputed S, dP
-# and B of the last two are not counted.  Forward 2 (S, PV); first backward
+# (8).  Pass 1 runs as two sweeps: U1-and-Y (the five score GEMMs + U1 x2 +
+# Y x2 = 9) and Z (one GEMM doing the work of U2 and W: 2); the recomputed S
+# and dP of the Z sweep are not counted.  Forward 2 (S, PV); first backward
 # 5 (S, dP, dQ in the row kernel, dV, dK in the column kernel; the column
 # kernel's recomputed S and dP are not counted).
-COUNTED_GEMMS = {"bob_pass1_u1": 7, "bob_pass1_z": 2, "bob_pass1_y": 2, "bob_pass2": 8,
+COUNTED_GEMMS = {"bob_pass1_u1y": 9, "bob_pass1_z": 2, "bob_pass2": 8,
                  "attn_fwd": 2, "attn_bwd_dq": 3, "attn_bwd_dkdv": 2}
 
 
@@ -65,8 +65,41 @@ def dist_env():
     return ws, rank, local
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (libnvidia-ml ships with the
+    driver): SM clock, its maximum and the active clock-event reasons."""
+    SM = 1                                                  # NVML_CLOCK_SM
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, index):
+        import ctypes
+        self.c = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib, self.h = lib, ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.sample()
+
+    def max_sm(self):
+        v = self.c.c_uint()
+        return float(v.value) if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM, self.c.byref(v)) == 0 else 0.0
+
+    def sample(self):
+        clk, r = self.c.c_uint(), self.c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, self.c.byref(clk)) != 0:
+            raise OSError("nvmlDeviceGetClockInfo failed")
+        self.reasons_fn(self.h, self.c.byref(r))
+        return float(clk.value), [n for n, bit in self.BITS.items() if r.value & bit]
+
+
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """SM clock and throttle reasons sampled DURING the timed region: an NVML
+    poller thread (every 2 ms, so short regions get samples too), else
+    nvidia-smi -lms 200.  Samples go to gpurun_out/clocks_rank<i>.csv."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -74,11 +107,32 @@ class Clocks:
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.nvml = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
 
     def start(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.nvml = _Nvml(self.index)
+        except Exception:
+            self.nvml = None
+        if self.nvml is not None:
+            import threading
+            self.samples, self.halt, self.live = [], threading.Event(), threading.Event()
+
+            def poll():
+                while not self.halt.is_set():
+                    if self.live.is_set():
+                        try:
+                            self.samples.append(self.nvml.sample())
+                        except Exception:
+                            return
+                    self.halt.wait(0.002)
+
+            self.thread = threading.Thread(target=poll, daemon=True)
+            self.thread.start()
+            return
+        try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
@@ -86,7 +140,25 @@ class Clocks:
         except Exception:
             self.proc = None
 
+    def begin(self):
+        """The timed region starts now (the NVML poller records from here on)."""
+        if self.nvml is not None:
+            self.live.set()
+
     def stop(self):
+        if self.nvml is not None:
+            self.halt.set()
+            self.thread.join(timeout=5)
+            mx = self.nvml.max_sm()
+            with open(self.path, "w") as f:
+                f.write("sm_mhz,sm_max_mhz,reasons\n")
+                for clk, rs in self.samples:
+                    f.write(f"{clk:.0f},{mx:.0f},{'|'.join(rs)}\n")
+            if not self.samples:
+                return None
+            reasons = sorted({n for _, rs in self.samples for n in rs})
+            return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": mx, "reasons": reasons,
+                    "samples": len(self.samples), "source": "nvml"}
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -112,7 +184,7 @@ class Clocks:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi"}
 
 
 def run_ours(args, w):
@@ -169,6 +241,7 @@ def run_ours(args, w):
     fb.fbob_profile_enable(True)      # per-kernel CUDA events on the launching stream
     barrier()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.begin()
     t0.record(stream)
     for _ in range(args.steps):
         step()

@@ -23,17 +23,18 @@
 // known, EX U2 + alpha W = sum_j (EX P + alpha dS) K_j, so
 //   gQ = tau (U1 - Z),  Z = sum_j G K_j,  G = EX P + alpha dS.
 //
-// Every score MMA reads its resident operand (Q, UQ, dO in pass 1; K, UK and,
-// at d = 64, V, UV in pass 2) from TMEM, so only the streamed 32-row tile is
-// read from shared memory.  TMEM (512 columns x 128 lanes fp32) then holds
-// one accumulator set per kernel, so pass 1 runs as three kernels over the
-// same 128-row blocks, in stream order:
-//   U1 kernel  U1 (d) | [S|B|dP|C] | (dS, X) halves | Q, UQ, dO
-//              writes U1 into gQ and (alpha, E) into the workspace;
+// The score MMAs read their resident operands (Q, UQ and, at d = 64, dO in
+// pass 1; K, UK and, at d = 64, V, UV in pass 2) from TMEM where it has room,
+// so mostly only the streamed 32-row tile is read from shared memory.  TMEM
+// (512 columns x 128 lanes fp32) holds one kernel's accumulators, so pass 1
+// runs as two kernels over the same 128-row blocks, in stream order:
+//   U1-and-Y kernel  U1, Y (2d) | [S|B|dP|C] x NBUF | Q, UQ (, dO)
+//              (the dS, X, P, PB operands in shared memory; at d = 128 one
+//              score buffer, dO in shared memory)
+//              writes U1 into gQ, (alpha, E) into the workspace and
+//              gdO = Y - alpha O;
 //   Z kernel   Z (d) | [S|dP] x 2 | G halves | Q, dO
-//              reads (alpha, E) and U1, writes gQ = tau (U1 - Z);
-//   Y kernel   Y (d) | [S|B] x 2 | (P, PB) halves | Q, UQ
-//              writes gdO = Y - alpha O (alpha summed again from P B).
+//              reads (alpha, E) and U1, writes gQ = tau (U1 - Z).
 // Pass 2: gK, gV (2d) | [S|B|dP|C] | then, at d = 64, the (dS, Gs, Gdp)
 // halves and K, UK, V, UV; at d = 128, K and UK (V, UV stay in shared memory
 // and the three operands go to shared memory).
@@ -53,9 +54,9 @@ using namespace tc;
 using namespace tile;
 
 struct P1Params {
-  CUtensorMap mK, mUK, mV, mUV;              // streamed, box {64, 32} (U1 sweep)
-  CUtensorMap mK64, mUK64, mV64, mUV64;      // streamed, box {64, 64} (Z and Y sweeps)
-  CUtensorMap mdO_res;                       // resident, box {64, 128} (U1 sweep at d = 128)
+  CUtensorMap mK, mUK, mV, mUV;              // streamed, box {64, 32} (U1-and-Y sweep)
+  CUtensorMap mK64, mV64;                    // streamed, box {64, 64} (Z sweep)
+  CUtensorMap mdO_res;                       // resident, box {64, 128} (U1-and-Y sweep at d = 128)
   const __nv_bfloat16 *Q, *UQ, *dO;          // resident (copied into TMEM)
   const float *L, *D, *O;
   float *gQ, *gdO, *ws;
@@ -92,29 +93,34 @@ __device__ __forceinline__ void load_tile2(const CUtensorMap* m0, const CUtensor
   }
 }
 
-// U1 sweep (32 keys per tile): U1 += dS UK + X K, alpha, EX.  Ring A = [K UK]
-// (also read by the accumulator MMAs), ring B = [V UV].  At d = 64 Q, UQ, dO
-// and the dS, X operands sit in TMEM; at d = 128 dO and the operands move to
-// shared memory, which leaves TMEM room for two score buffers.
+// U1-and-Y sweep (32 keys per tile): U1 += dS UK + X K, Y += P UV + PB V,
+// alpha, EX; writes U1 (into gQ, finished by the Z sweep), (alpha, E) and
+// gdO = Y - alpha O.  Ring A = [K UK V UV] (all read by the accumulator
+// MMAs).  The four operands dS, X, P, PB go to shared memory.  At d = 128,
+// Q and UQ sit in TMEM and dO in shared memory, with one score buffer whose
+// columns the two warpgroups split; at d = 64 Q, UQ, dO sit in TMEM with two
+// score buffers.
 template <int D_>
-struct PassU1 {
+struct PassU1Y {
   using Params = P1Params;
-  static constexpr bool SPLIT = false, ROWS = true;
   static constexpr int D = D_, DC = D / 64, T = 32;
   static constexpr bool kWide = D == 128;
+  static constexpr bool ROWS = true, SPLIT = kWide;
   static constexpr int TRES = kWide ? 2 : 3;            // Q, UQ (, dO)
   static constexpr int RES = kWide ? DC * kChunk : 0;   // dO in shared memory
-  static constexpr int ACH = 2 * kBlk, BCH = 2 * kBlk;
-  static constexpr int SA = DC * ACH, SB = DC * BCH, SA_TX = SA, SB_TX = SB;
-  static constexpr int NSA = kWide ? 5 : 8, NSB = NSA;
-  static constexpr bool VEC = false, ROW_SUMS = true, TS = !kWide;
+  static constexpr int ACH = 4 * kBlk;                  // [K | UK | V | UV] per 64-column chunk
+  static constexpr int SA = DC * ACH, SA_TX = SA, SB = 0, SB_TX = 0;
+  static constexpr int NSA = kWide ? 4 : 8, NSB = 0;
+  static constexpr bool VEC = false, ROW_SUMS = true, TS = false;
   static constexpr int VEC_OFF = 0, NVEC = 0, VEC_SCRATCH = 0;
-  static constexpr int OPS = kWide ? 2 * kChunk : 0;    // dS, X tiles; half h = columns 32h..32h+31
-  static constexpr int ACC = D, SCOLS = 128, NBUF = 2;  // [S|B|dP|C]
-  static constexpr int OP_HALF = 32;                    // TMEM operands dS, X
-  static constexpr int OP_COL = ACC + NBUF * SCOLS;
-  static constexpr int TRES_COL = OP_COL + (TS ? 2 * OP_HALF : 0);
-  static constexpr int SMEM = RES + NSA * SA + NSB * SB + OPS;
+  static constexpr int OPS = 4 * kChunk;                // dS, X, P, PB tiles; half h = columns 32h..32h+31
+  static constexpr int ACC = 2 * D;                     // U1 | Y
+  static constexpr int SCOLS = 128, NBUF = kWide ? 1 : 2;   // [S|B|dP|C]
+  static constexpr int OP_HALF = 0, OP_COL = ACC + NBUF * SCOLS;
+  static constexpr int TRES_COL = OP_COL;
+  static constexpr int SMEM = RES + NSA * SA + OPS;
+  static constexpr int A_U1 = 0, A_Y = D;
+  static constexpr int NC = SPLIT ? T / 2 : T;          // key columns per warpgroup and tile
   static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
   static_assert(SMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
 
@@ -126,12 +132,12 @@ struct PassU1 {
   }
   __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head, bool) {
     load_tile2(&p.mK, &p.mUK, st, DC, ACH, kBlk, bar, t * T, head);
+    load_tile2(&p.mV, &p.mUV, st + 2 * kBlk, DC, ACH, kBlk, bar, t * T, head);
   }
+  __device__ static void load_b(const Params&, uint8_t*, uint64_t*, int, int) {}
   __device__ static void fill_vec(const Params&, float*, int, int, int) {}
-  __device__ static void load_b(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
-    load_tile2(&p.mV, &p.mUV, st, DC, BCH, kBlk, bar, t * T, head);
-  }
-  __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t res, uint32_t sa, uint32_t sb) {
+
+  __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t res, uint32_t sa, uint32_t) {
     const uint32_t i64 = idesc_bf16(kM, 64, false, false), i32 = idesc_bf16(kM, 32, false, false);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k)  // [S | Q UK^T] = Q [K; UK]^T
@@ -142,9 +148,9 @@ struct PassU1 {
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {  // [dP | C] = dO [V; UV]^T
       if (kWide)
-        mma_ss_w(sc + 64, res_lo(res, 0, DC, k), kmaj(sb, BCH, 0, k), i64, k > 0);
+        mma_ss_w(sc + 64, res_lo(res, 0, DC, k), kmaj(sa, ACH, 2 * kBlk, k), i64, k > 0);
       else
-        mma_ts_w(sc + 64, tres_a(tres, 2, D, k), kmaj(sb, BCH, 0, k), i64, k > 0);
+        mma_ts_w(sc + 64, tres_a(tres, 2, D, k), kmaj(sa, ACH, 2 * kBlk, k), i64, k > 0);
     }
   }
   __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
@@ -153,14 +159,10 @@ struct PassU1 {
 #pragma unroll
     for (int kk = 0; kk < T / 16; ++kk) {
       const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
-      if (kWide) {
-        mma_ss_w(tb, op_lo(ops, 0, h, kk), mnmaj(amn, kBlk, kk), id, acc0);  // U1 += dS UK
-        mma_ss_w(tb, op_lo(ops, 1, h, kk), mnmaj(amn, 0, kk), id, 1);        // U1 += X K
-      } else {
-        const uint32_t a = ops + h * OP_HALF + kk * 8;
-        mma_ts_w(tb, a, mnmaj(amn, kBlk, kk), id, acc0);
-        mma_ts_w(tb, a + 16, mnmaj(amn, 0, kk), id, 1);
-      }
+      mma_ss_w(tb + A_U1, op_lo(ops, 0, h, kk), mnmaj(amn, kBlk, kk), id, acc0);     // U1 += dS UK
+      mma_ss_w(tb + A_U1, op_lo(ops, 1, h, kk), mnmaj(amn, 0, kk), id, 1);           // U1 += X K
+      mma_ss_w(tb + A_Y, op_lo(ops, 2, h, kk), mnmaj(amn, 3 * kBlk, kk), id, acc0);  // Y += P UV
+      mma_ss_w(tb + A_Y, op_lo(ops, 3, h, kk), mnmaj(amn, 2 * kBlk, kk), id, 1);     // Y += PB V
     }
   }
   struct Row {
@@ -174,40 +176,50 @@ struct PassU1 {
     w.alpha = 0.f;
     w.ex = 0.f;
   }
+  // Operands are written 16 columns at a time.  With two score buffers the
+  // operand half is acquired first (as in the dK/dV kernel); with one (split
+  // columns, a single 16-column chunk per warpgroup) the scores are released
+  // first so the next tile's score MMAs can start.
+  static constexpr bool kEarly = NBUF > 1;
+  static_assert(kEarly || NC == 16, "late acquire needs a single chunk");
   template <bool MASK>
   __device__ static bool ew_tile(Row& w, const Params& p, const TileArgs& a, const TileSync& s, int r) {
     const float sc = p.tau * kLog2e;
-    uint32_t wdS[16], wX[16];
+    if (kEarly && !s.acquire_ops()) return false;
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < NC / 16; ++q) {
       float S[16], B[16], dP[16], C[16];
-      tmem_ld16x4(a.sc + q * 16, a.sc + 32 + q * 16, a.sc + 64 + q * 16, a.sc + 96 + q * 16, S, B, dP, C);
-      if (q == 1) s.release_scores();
+      const uint32_t c = a.sc + a.c0 + q * 16;
+      tmem_ld16x4(c, c + 32, c + 64, c + 96, S, B, dP, C);
+      if (q == NC / 16 - 1) s.release_scores();
+      uint32_t wdS[8], wX[8], wP[8], wPB[8];
 #pragma unroll
       for (int j = 0; j < 16; j += 2) {
-        float ds[2], x[2];
+        float ds[2], x[2], pv[2], pb[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int col = q * 16 + j + e;   // tile column (key)
+          const int col = a.c0 + q * 16 + j + e;   // tile column (key)
           const float pe = (!MASK || (col >= a.lo && col <= a.hi)) ? ex2(fmaf(S[j + e], sc, w.nL)) : 0.f;
           const float be = p.tau * B[j + e];
           const float te = dP[j + e] - w.Di;
-          w.alpha = fmaf(pe, be, w.alpha);
+          pv[e] = pe;
+          pb[e] = pe * be;
+          w.alpha += pb[e];
           ds[e] = pe * te;
           x[e] = pe * fmaf(be, te, C[j + e]);
           w.ex += x[e];
         }
-        wdS[q * 8 + j / 2] = pack_bf16x2(ds[0], ds[1]);
-        wX[q * 8 + j / 2] = pack_bf16x2(x[0], x[1]);
+        wdS[j / 2] = pack_bf16x2(ds[0], ds[1]);
+        wX[j / 2] = pack_bf16x2(x[0], x[1]);
+        wP[j / 2] = pack_bf16x2(pv[0], pv[1]);
+        wPB[j / 2] = pack_bf16x2(pb[0], pb[1]);
       }
-    }
-    if (!s.acquire_ops()) return false;
-    if (kWide) {
-      write_op_half(a.ops, (uint32_t)r, a.h, wdS);
-      write_op_half(a.ops + kChunk, (uint32_t)r, a.h, wX);
-    } else {
-      tmem_st16_nowait(a.ops, wdS);
-      tmem_st16_nowait(a.ops + 16, wX);
+      if (!kEarly && !s.acquire_ops()) return false;
+      const int col = 32 * (int)a.h + a.c0 + q * 16;
+      write_op_cols<8>(a.ops, (uint32_t)r, col, wdS);
+      write_op_cols<8>(a.ops + kChunk, (uint32_t)r, col, wX);
+      write_op_cols<8>(a.ops + 2 * kChunk, (uint32_t)r, col, wP);
+      write_op_cols<8>(a.ops + 3 * kChunk, (uint32_t)r, col, wPB);
     }
     s.publish_ops();
     return true;
@@ -215,16 +227,27 @@ struct PassU1 {
   __device__ static void epilogue(Row& w, const Params& p, const EpiArgs& e) {
     float alpha = w.alpha, ex = w.ex;
     if (!e.sum_rows(alpha, ex)) return;
-    // every lane runs the (warp-collective) TMEM loads; rows >= N store nothing
+    // every lane runs the (warp-collective) TMEM loads; rows >= N touch no memory
     const bool keep = e.blk0 + e.r < p.N;
     const size_t vo = (size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0);
     const size_t ro = vo * D;
     const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
 #pragma unroll 1
     for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
-      float acc[16];
-      tmem_ld16(e.tm + c0, acc);
-      if (keep) store16(p.gQ + ro + c0, acc);   // U1, finished by the Z sweep
+      float u1[16], y[16], o[16];
+      tmem_ld16x2(e.tm + A_U1 + c0, e.tm + A_Y + c0, u1, y);
+      if (!keep) continue;
+      store16(p.gQ + ro + c0, u1);   // U1, finished by the Z sweep
+      const float4* src = reinterpret_cast<const float4*>(p.O + ro + c0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = src[q];
+        o[4 * q] = fmaf(-alpha, v.x, y[4 * q]);          // gdO = Y - alpha O
+        o[4 * q + 1] = fmaf(-alpha, v.y, y[4 * q + 1]);
+        o[4 * q + 2] = fmaf(-alpha, v.z, y[4 * q + 2]);
+        o[4 * q + 3] = fmaf(-alpha, v.w, y[4 * q + 3]);
+      }
+      store16(p.gdO + ro + c0, o);
     }
     if (keep && e.g == 0) {
       p.ws[2 * vo] = alpha;
@@ -291,7 +314,7 @@ struct PassZ {
     const size_t vo = (size_t)head * p.N + (ok ? blk0 + r : 0);
     w.nL = ok ? -p.L[vo] * kLog2e : 0.f;
     w.Di = ok ? p.D[vo] : 0.f;
-    w.alpha = ok ? p.ws[2 * vo] : 0.f;                            // row totals of the U1 sweep
+    w.alpha = ok ? p.ws[2 * vo] : 0.f;                            // row totals of the U1-and-Y sweep
     w.ex = ok ? fmaf(-w.Di, w.alpha, p.ws[2 * vo + 1]) : 0.f;     // EX = E - D alpha
   }
   template <bool MASK>
@@ -345,119 +368,6 @@ struct PassZ {
         o[4 * q + 3] = p.tau * (v.w - z[4 * q + 3]);
       }
       store16(p.gQ + ro + c0, o);
-    }
-  }
-};
-
-// Y sweep: Y += P UV + PB V, alpha; gdO = Y - alpha O.  Ring A = [V UV]
-// (read by the accumulator MMAs), ring B = [K UK].  P and PB go to TMEM; 64
-// keys per tile at d = 64, 32 at d = 128 (two score buffers either way).
-template <int D_>
-struct PassY {
-  using Params = P1Params;
-  static constexpr bool SPLIT = false, ROWS = true;
-  static constexpr int D = D_, DC = D / 64, T = D == 128 ? 32 : 64, BLK = T * 128;
-  static constexpr int RES = 0, TRES = 2;   // Q, UQ
-  static constexpr int ACH = 2 * BLK, BCH = 2 * BLK;
-  static constexpr int SA = DC * ACH, SB = DC * BCH, SA_TX = SA, SB_TX = SB;
-  static constexpr int NSA = 6, NSB = NSA;
-  static constexpr bool VEC = false, ROW_SUMS = true, TS = true;
-  static constexpr int VEC_OFF = 0, OPS = 0, NVEC = 0, VEC_SCRATCH = 0;
-  static constexpr int ACC = D, SCOLS = 2 * T, NBUF = 2;   // [S | B]
-  static constexpr int OP_HALF = T;                     // P, PB (32 columns each)
-  static constexpr int OP_COL = ACC + NBUF * SCOLS;
-  static constexpr int TRES_COL = OP_COL + 2 * OP_HALF;
-  static constexpr int SMEM = NSA * SA + NSB * SB;
-  static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
-  static_assert(SMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
-
-  __device__ static const void* tres_src(const Params& p, int s) { return s == 0 ? (const void*)p.Q : (const void*)p.UQ; }
-  __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
-  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head, bool) {
-    load_tile2(T == 64 ? &p.mV64 : &p.mV, T == 64 ? &p.mUV64 : &p.mUV, st, DC, ACH, BLK, bar, t * T, head);
-  }
-  __device__ static void fill_vec(const Params&, float*, int, int, int) {}
-  __device__ static void load_b(const Params& p, uint8_t* st, uint64_t* bar, int t, int head) {
-    load_tile2(T == 64 ? &p.mK64 : &p.mK, T == 64 ? &p.mUK64 : &p.mUK, st, DC, BCH, BLK, bar, t * T, head);
-  }
-  __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t, uint32_t, uint32_t sb) {
-    const uint32_t i128 = idesc_bf16(kM, 2 * T, false, false), i64 = idesc_bf16(kM, T, false, false);
-#pragma unroll
-    for (int k = 0; k < D / 16; ++k)  // [S | Q UK^T] = Q [K; UK]^T
-      mma_ts_w(sc, tres_a(tres, 0, D, k), kmaj(sb, BCH, 0, k), i128, k > 0);
-#pragma unroll
-    for (int k = 0; k < D / 16; ++k)  // B += UQ K^T
-      mma_ts_w(sc + T, tres_a(tres, 1, D, k), kmaj(sb, BCH, 0, k), i64, 1);
-  }
-  __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
-    const uint32_t amn = desc_lo(sa, ACH);
-    const uint32_t id = idesc_bf16(kM, D, false, true);
-#pragma unroll
-    for (int kk = 0; kk < T / 16; ++kk) {
-      const uint32_t a = ops + h * OP_HALF + kk * 8;
-      mma_ts_w(tb, a, mnmaj(amn, BLK, kk), id, (first && kk == 0) ? 0u : 1u);  // Y += P UV
-      mma_ts_w(tb, a + T / 2, mnmaj(amn, 0, kk), id, 1);                        // Y += PB V
-    }
-  }
-  struct Row {
-    float nL, alpha;
-  };
-  __device__ static void ew_init(Row& w, const Params& p, int blk0, int r, int head) {
-    w.nL = blk0 + r < p.N ? -p.L[(size_t)head * p.N + blk0 + r] * kLog2e : 0.f;
-    w.alpha = 0.f;
-  }
-  template <bool MASK>
-  __device__ static bool ew_tile(Row& w, const Params& p, const TileArgs& a, const TileSync& s, int) {
-    const float sc = p.tau * kLog2e;
-    // operands written chunk by chunk (see the dK/dV kernel)
-    if (!s.acquire_ops()) return false;
-#pragma unroll
-    for (int q = 0; q < T / 16; ++q) {
-      float S[16], B[16];
-      tmem_ld16x2(a.sc + q * 16, a.sc + T + q * 16, S, B);
-      if (q == T / 16 - 1) s.release_scores();
-      uint32_t wP[8], wPB[8];
-#pragma unroll
-      for (int j = 0; j < 16; j += 2) {
-        float pv[2], pb[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int col = q * 16 + j + e;   // tile column (key)
-          pv[e] = (!MASK || (col >= a.lo && col <= a.hi)) ? ex2(fmaf(S[j + e], sc, w.nL)) : 0.f;
-          pb[e] = pv[e] * (p.tau * B[j + e]);
-          w.alpha += pb[e];
-        }
-        wP[j / 2] = pack_bf16x2(pv[0], pv[1]);
-        wPB[j / 2] = pack_bf16x2(pb[0], pb[1]);
-      }
-      tmem_st8_nowait(a.ops + 8 * q, wP);
-      tmem_st8_nowait(a.ops + T / 2 + 8 * q, wPB);
-    }
-    s.publish_ops();
-    return true;
-  }
-  __device__ static void epilogue(Row& w, const Params& p, const EpiArgs& e) {
-    float alpha = w.alpha, unused = 0.f;
-    if (!e.sum_rows(alpha, unused)) return;
-    // every lane runs the (warp-collective) TMEM loads; rows >= N touch no memory
-    const bool keep = e.blk0 + e.r < p.N;
-    const size_t ro = ((size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0)) * D;
-    const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
-#pragma unroll 1
-    for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
-      float y[16], o[16];
-      tmem_ld16(e.tm + c0, y);
-      if (!keep) continue;
-      const float4* src = reinterpret_cast<const float4*>(p.O + ro + c0);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v = src[q];
-        o[4 * q] = fmaf(-alpha, v.x, y[4 * q]);
-        o[4 * q + 1] = fmaf(-alpha, v.y, y[4 * q + 1]);
-        o[4 * q + 2] = fmaf(-alpha, v.z, y[4 * q + 2]);
-        o[4 * q + 3] = fmaf(-alpha, v.w, y[4 * q + 3]);
-      }
-      store16(p.gdO + ro + c0, o);
     }
   }
 };
@@ -674,8 +584,7 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   const int BH = a.BH, N = a.N;
   bool ok = make_bf16_map(&p1.mK, a.K, BH, N, D, kT) && make_bf16_map(&p1.mUK, a.UK, BH, N, D, kT) &&
             make_bf16_map(&p1.mV, a.V, BH, N, D, kT) && make_bf16_map(&p1.mUV, a.UV, BH, N, D, kT) &&
-            make_bf16_map(&p1.mK64, a.K, BH, N, D, 64) && make_bf16_map(&p1.mUK64, a.UK, BH, N, D, 64) &&
-            make_bf16_map(&p1.mV64, a.V, BH, N, D, 64) && make_bf16_map(&p1.mUV64, a.UV, BH, N, D, 64) &&
+            make_bf16_map(&p1.mK64, a.K, BH, N, D, 64) && make_bf16_map(&p1.mV64, a.V, BH, N, D, 64) &&
             make_bf16_map(&p1.mdO_res, a.dO, BH, N, D, kM);
   if (!ok) return cudaErrorInvalidValue;
   p1.Q = static_cast<const __nv_bfloat16*>(a.Q);
@@ -694,10 +603,9 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   p1.wait_ns = c.wait_ns;
   p1.stall = c.stall;
   const dim3 grid((N + kM - 1) / kM, BH);
-  // the Z kernel reads what the U1 kernel wrote (U1 in gQ, alpha and E)
-  cudaError_t e = launch<PassU1<D>>("bob_pass1_u1", p1, grid, s);
+  // the Z kernel reads what the U1-and-Y kernel wrote (U1 in gQ, alpha and E)
+  cudaError_t e = launch<PassU1Y<D>>("bob_pass1_u1y", p1, grid, s);
   if (e == cudaSuccess) e = launch<PassZ<D>>("bob_pass1_z", p1, grid, s);
-  if (e == cudaSuccess) e = launch<PassY<D>>("bob_pass1_y", p1, grid, s);
   if (e != cudaSuccess) return e;
   P2Params p2;
   ok = make_bf16_map(&p2.mQ, a.Q, BH, N, D, kT) && make_bf16_map(&p2.mUQ, a.UQ, BH, N, D, kT) &&
