@@ -43,7 +43,8 @@ fbob_status check_problem(const fbob_problem* p, bool* empty) {
     return fail(FBOB_ERR_INVALID_ARG, "tau must be finite and nonzero (got %g)", (double)p->tau);
   if (p->dtype != FBOB_BF16 && p->dtype != FBOB_FP32)
     return fail(FBOB_ERR_INVALID_ARG, "unknown dtype %d", p->dtype);
-  if (p->d != 64 && p->d != 128) return fail(FBOB_ERR_UNSUPPORTED, "head size d=%d (supported: 64, 128)", p->d);
+  if (p->d != 32 && p->d != 64 && p->d != 96 && p->d != 128)
+    return fail(FBOB_ERR_UNSUPPORTED, "head size d=%d (supported: 32, 64, 96, 128)", p->d);
   const long long heads = (long long)p->B * p->H;
   if (heads > 65535) return fail(FBOB_ERR_UNSUPPORTED, "B*H=%lld exceeds 65535", heads);
   if ((long long)p->N * p->d * heads > (1ll << 40))

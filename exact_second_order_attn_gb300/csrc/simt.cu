@@ -524,13 +524,28 @@ cudaError_t bob_t(const BobArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t simt_fwd(const FwdArgs& a, const DevCtx&, cudaStream_t s) {
-  return a.d == 64 ? fwd_t<float, 64>(a, s) : fwd_t<float, 128>(a, s);
+  switch (a.d) {
+    case 32: return fwd_t<float, 32>(a, s);
+    case 64: return fwd_t<float, 64>(a, s);
+    case 96: return fwd_t<float, 96>(a, s);
+    default: return fwd_t<float, 128>(a, s);
+  }
 }
 cudaError_t simt_bwd(const BwdArgs& a, const DevCtx&, cudaStream_t s) {
-  return a.d == 64 ? bwd_t<float, 64>(a, s) : bwd_t<float, 128>(a, s);
+  switch (a.d) {
+    case 32: return bwd_t<float, 32>(a, s);
+    case 64: return bwd_t<float, 64>(a, s);
+    case 96: return bwd_t<float, 96>(a, s);
+    default: return bwd_t<float, 128>(a, s);
+  }
 }
 cudaError_t simt_bob(const BobArgs& a, const DevCtx&, cudaStream_t s) {
-  return a.d == 64 ? bob_t<float, 64>(a, s) : bob_t<float, 128>(a, s);
+  switch (a.d) {
+    case 32: return bob_t<float, 32>(a, s);
+    case 64: return bob_t<float, 64>(a, s);
+    case 96: return bob_t<float, 96>(a, s);
+    default: return bob_t<float, 128>(a, s);
+  }
 }
 
 }  // namespace fbob

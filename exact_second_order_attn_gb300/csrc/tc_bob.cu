@@ -61,6 +61,7 @@ struct P1Params {
   const float *L, *D, *O;
   float *gQ, *gdO, *ws;
   int N;
+  int dv;                                    // head size in global memory (<= D; see tc_tile.cuh)
   float tau;
   int causal;
   unsigned int* err;
@@ -75,6 +76,7 @@ struct P2Params {
   const float *L, *D, *ws;
   float *gK, *gV;
   int N;
+  int dv;                                    // head size in global memory (<= D; see tc_tile.cuh)
   float tau;
   int causal;
   unsigned int* err;
@@ -230,8 +232,8 @@ struct PassU1Y {
     // every lane runs the (warp-collective) TMEM loads; rows >= N touch no memory
     const bool keep = e.blk0 + e.r < p.N;
     const size_t vo = (size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0);
-    const size_t ro = vo * D;
-    const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
+    const size_t ro = vo * p.dv;
+    const int c_lo = e.g * (D / 2), c_hi = min(c_lo + D / 2, p.dv);   // columns >= dv hold zeros
 #pragma unroll 1
     for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
       float u1[16], y[16], o[16];
@@ -351,8 +353,8 @@ struct PassZ {
   __device__ static void epilogue(Row&, const Params& p, const EpiArgs& e) {
     // every lane runs the (warp-collective) TMEM loads; rows >= N touch no memory
     const bool keep = e.blk0 + e.r < p.N;
-    const size_t ro = ((size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0)) * D;
-    const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
+    const size_t ro = ((size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0)) * p.dv;
+    const int c_lo = e.g * (D / 2), c_hi = min(c_lo + D / 2, p.dv);   // columns >= dv hold zeros
 #pragma unroll 1
     for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
       float z[16], o[16];
@@ -545,8 +547,8 @@ struct Pass2 {
   __device__ static void epilogue(Row&, const Params& p, const EpiArgs& e) {
     // every lane runs the (warp-collective) TMEM loads; rows >= N store nothing
     const bool keep = e.blk0 + e.r < p.N;
-    const size_t ro = ((size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0)) * D;
-    const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
+    const size_t ro = ((size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0)) * p.dv;
+    const int c_lo = e.g * (D / 2), c_hi = min(c_lo + D / 2, p.dv);   // columns >= dv hold zeros
 #pragma unroll 1
     for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
       float ak[16], av[16];
@@ -582,10 +584,10 @@ template <int D>
 cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   P1Params p1;
   const int BH = a.BH, N = a.N;
-  bool ok = make_bf16_map(&p1.mK, a.K, BH, N, D, kT) && make_bf16_map(&p1.mUK, a.UK, BH, N, D, kT) &&
-            make_bf16_map(&p1.mV, a.V, BH, N, D, kT) && make_bf16_map(&p1.mUV, a.UV, BH, N, D, kT) &&
-            make_bf16_map(&p1.mK64, a.K, BH, N, D, 64) && make_bf16_map(&p1.mV64, a.V, BH, N, D, 64) &&
-            make_bf16_map(&p1.mdO_res, a.dO, BH, N, D, kM);
+  bool ok = make_bf16_map(&p1.mK, a.K, BH, N, a.d, kT) && make_bf16_map(&p1.mUK, a.UK, BH, N, a.d, kT) &&
+            make_bf16_map(&p1.mV, a.V, BH, N, a.d, kT) && make_bf16_map(&p1.mUV, a.UV, BH, N, a.d, kT) &&
+            make_bf16_map(&p1.mK64, a.K, BH, N, a.d, 64) && make_bf16_map(&p1.mV64, a.V, BH, N, a.d, 64) &&
+            make_bf16_map(&p1.mdO_res, a.dO, BH, N, a.d, kM);
   if (!ok) return cudaErrorInvalidValue;
   p1.Q = static_cast<const __nv_bfloat16*>(a.Q);
   p1.UQ = static_cast<const __nv_bfloat16*>(a.UQ);
@@ -597,6 +599,7 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   p1.gdO = a.gdO;
   p1.ws = a.ws;
   p1.N = N;
+  p1.dv = a.d;
   p1.tau = a.tau;
   p1.causal = a.causal;
   p1.err = c.err;
@@ -608,9 +611,9 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   if (e == cudaSuccess) e = launch<PassZ<D>>("bob_pass1_z", p1, grid, s);
   if (e != cudaSuccess) return e;
   P2Params p2;
-  ok = make_bf16_map(&p2.mQ, a.Q, BH, N, D, kT) && make_bf16_map(&p2.mUQ, a.UQ, BH, N, D, kT) &&
-       make_bf16_map(&p2.mdO, a.dO, BH, N, D, kT) && make_bf16_map(&p2.mV, a.V, BH, N, D, kM) &&
-       make_bf16_map(&p2.mUV, a.UV, BH, N, D, kM);
+  ok = make_bf16_map(&p2.mQ, a.Q, BH, N, a.d, kT) && make_bf16_map(&p2.mUQ, a.UQ, BH, N, a.d, kT) &&
+       make_bf16_map(&p2.mdO, a.dO, BH, N, a.d, kT) && make_bf16_map(&p2.mV, a.V, BH, N, a.d, kM) &&
+       make_bf16_map(&p2.mUV, a.UV, BH, N, a.d, kM);
   if (!ok) return cudaErrorInvalidValue;
   p2.K = static_cast<const __nv_bfloat16*>(a.K);
   p2.UK = static_cast<const __nv_bfloat16*>(a.UK);
@@ -622,6 +625,7 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   p2.gK = a.gK;
   p2.gV = a.gV;
   p2.N = N;
+  p2.dv = a.d;
   p2.tau = a.tau;
   p2.causal = a.causal;
   p2.err = c.err;
@@ -633,7 +637,8 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
 }  // namespace
 
 cudaError_t tc_bob(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
-  return a.d == 64 ? bob_d<64>(a, c, s) : bob_d<128>(a, c, s);
+  // d = 32, 96 run on the d = 64, 128 kernels with zero-padded columns
+  return a.d <= 64 ? bob_d<64>(a, c, s) : bob_d<128>(a, c, s);
 }
 
 }  // namespace fbob

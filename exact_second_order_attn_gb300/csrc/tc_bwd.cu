@@ -34,6 +34,7 @@ struct DqParams {
   const float *O, *L;
   float *dQ, *D;
   int N;
+  int dv;                  // head size in global memory (<= D; see tc_tile.cuh)
   float tau;
   int causal;
   unsigned int* err;
@@ -101,13 +102,13 @@ struct DqOp {
     w.nL = 0.f;
     if (blk0 + r >= p.N) return;   // ragged N: row past the end (never stored)
     const size_t vo = (size_t)head * p.N + blk0 + r;
-    const size_t ro = vo * D;
+    const size_t ro = vo * p.dv;
     // D_i = rowsum(dO o O) of this thread's row
     float Di = 0.f;
     const uint4* g = reinterpret_cast<const uint4*>(p.dO + ro);
     const float4* o = reinterpret_cast<const float4*>(p.O + ro);
 #pragma unroll 4
-    for (int c = 0; c < D / 8; ++c) {
+    for (int c = 0; c < p.dv / 8; ++c) {
       const uint4 u = g[c];
       const float4 o0 = o[2 * c], o1 = o[2 * c + 1];
       const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -156,8 +157,8 @@ struct DqOp {
   __device__ static void epilogue(Row&, const Params& p, const tile::EpiArgs& e) {
     // every lane runs the (warp-collective) TMEM loads; rows >= N store nothing
     const bool keep = e.blk0 + e.r < p.N;
-    const size_t ro = ((size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0)) * D;
-    const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
+    const size_t ro = ((size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0)) * p.dv;
+    const int c_lo = e.g * (D / 2), c_hi = min(c_lo + D / 2, p.dv);   // columns >= dv hold zeros
 #pragma unroll 1
     for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
       float v[16];
@@ -175,6 +176,7 @@ struct DkvParams {
   const float *L, *D;
   float *dK, *dV;
   int N;
+  int dv;                  // head size in global memory (<= D; see tc_tile.cuh)
   float tau;
   int causal;
   unsigned int* err;
@@ -293,8 +295,8 @@ struct DkvOp {
   __device__ static void epilogue(Row&, const Params& p, const tile::EpiArgs& e) {
     // every lane runs the (warp-collective) TMEM loads; rows >= N store nothing
     const bool keep = e.blk0 + e.r < p.N;
-    const size_t ro = ((size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0)) * D;
-    const int c_lo = e.g * (D / 2), c_hi = c_lo + D / 2;
+    const size_t ro = ((size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0)) * p.dv;
+    const int c_lo = e.g * (D / 2), c_hi = min(c_lo + D / 2, p.dv);   // columns >= dv hold zeros
 #pragma unroll 1
     for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
       float k_[16], v[16];
@@ -332,7 +334,7 @@ auto pick(bool causal, bool ragged) {
 template <int D>
 cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
   DqParams q;
-  if (!make_bf16_map(&q.mK, a.K, a.BH, a.N, D, DqOp<D>::T) || !make_bf16_map(&q.mV, a.V, a.BH, a.N, D, DqOp<D>::T))
+  if (!make_bf16_map(&q.mK, a.K, a.BH, a.N, a.d, DqOp<D>::T) || !make_bf16_map(&q.mV, a.V, a.BH, a.N, a.d, DqOp<D>::T))
     return cudaErrorInvalidValue;
   q.Q = static_cast<const __nv_bfloat16*>(a.Q);
   q.O = a.O;
@@ -341,6 +343,7 @@ cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
   q.dQ = a.dQ;
   q.D = a.D;
   q.N = a.N;
+  q.dv = a.d;
   q.tau = a.tau;
   q.causal = a.causal;
   q.err = c.err;
@@ -351,7 +354,7 @@ cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
   cudaError_t e = launch("attn_bwd_dq", pick<DqOp<D>>(a.causal, ragged), DqOp<D>::SMEM, tile::kThreads, grid, q, s);
   if (e != cudaSuccess) return e;
   DkvParams k;
-  if (!make_bf16_map(&k.mQ, a.Q, a.BH, a.N, D, DkvOp<D>::T) || !make_bf16_map(&k.mdO, a.dO, a.BH, a.N, D, DkvOp<D>::T))
+  if (!make_bf16_map(&k.mQ, a.Q, a.BH, a.N, a.d, DkvOp<D>::T) || !make_bf16_map(&k.mdO, a.dO, a.BH, a.N, a.d, DkvOp<D>::T))
     return cudaErrorInvalidValue;
   k.K = static_cast<const __nv_bfloat16*>(a.K);
   k.V = static_cast<const __nv_bfloat16*>(a.V);
@@ -360,6 +363,7 @@ cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
   k.dK = a.dK;
   k.dV = a.dV;
   k.N = a.N;
+  k.dv = a.d;
   k.tau = a.tau;
   k.causal = a.causal;
   k.err = c.err;
@@ -371,7 +375,8 @@ cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
 }  // namespace
 
 cudaError_t tc_bwd(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
-  return a.d == 64 ? bwd_d<64>(a, c, s) : bwd_d<128>(a, c, s);
+  // d = 32, 96 run on the d = 64, 128 kernels with zero-padded columns
+  return a.d <= 64 ? bwd_d<64>(a, c, s) : bwd_d<128>(a, c, s);
 }
 
 }  // namespace fbob

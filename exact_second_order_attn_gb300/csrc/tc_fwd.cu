@@ -43,6 +43,7 @@ struct FwdParams {
   CUtensorMap mQ, mK, mV;  // box {64, 128}
   float *O, *L;
   int N;
+  int dv;                  // head size in global memory (<= D; see tc_tile.cuh)
   float tau;
   int causal;
   unsigned int* err;
@@ -301,10 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc(const __grid_constant
       // every lane runs the (warp-collective) TMEM loads; rows >= N store nothing
       const int i = row0 + x * kM + r;
       const bool keep = i < p.N;
-      const size_t ro = ((size_t)head * p.N + (keep ? i : 0)) * D;
+      const size_t ro = ((size_t)head * p.N + (keep ? i : 0)) * p.dv;
       const float inv = 1.f / l;
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 16) {
+      for (int c0 = 0; c0 < p.dv; c0 += 16) {   // columns >= dv hold zeros
         float o[16];
         tmem_ld16(tb + lane + x * D + c0, o);
 #pragma unroll
@@ -325,12 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc(const __grid_constant
 template <int D>
 cudaError_t fwd_d(const FwdArgs& a, const DevCtx& c, cudaStream_t s) {
   FwdParams p;
-  if (!make_bf16_map(&p.mQ, a.Q, a.BH, a.N, D, kM) || !make_bf16_map(&p.mK, a.K, a.BH, a.N, D, kKT) ||
-      !make_bf16_map(&p.mV, a.V, a.BH, a.N, D, kKT))
+  if (!make_bf16_map(&p.mQ, a.Q, a.BH, a.N, a.d, kM) || !make_bf16_map(&p.mK, a.K, a.BH, a.N, a.d, kKT) ||
+      !make_bf16_map(&p.mV, a.V, a.BH, a.N, a.d, kKT))
     return cudaErrorInvalidValue;
   p.O = a.O;
   p.L = a.L;
   p.N = a.N;
+  p.dv = a.d;
   p.tau = a.tau;
   p.causal = a.causal;
   p.err = c.err;
@@ -351,7 +353,8 @@ cudaError_t fwd_d(const FwdArgs& a, const DevCtx& c, cudaStream_t s) {
 }  // namespace
 
 cudaError_t tc_fwd(const FwdArgs& a, const DevCtx& c, cudaStream_t s) {
-  return a.d == 64 ? fwd_d<64>(a, c, s) : fwd_d<128>(a, c, s);
+  // d = 32, 96 run on the d = 64, 128 kernels with zero-padded columns
+  return a.d <= 64 ? fwd_d<64>(a, c, s) : fwd_d<128>(a, c, s);
 }
 
 }  // namespace fbob

@@ -200,6 +200,12 @@ struct TileArgs {
 // of that last tile - of every tile when N is not a multiple of 4, since a
 // bulk copy needs a 16-byte aligned source and head h starts at float h N -
 // are read with bounds checks instead of a bulk copy.
+//
+// Narrower heads: a kernel built for D serves any head size p.dv <= D (a
+// multiple of 16): global rows are p.dv wide, TMA fills the box columns at or
+// beyond p.dv with zeros (the tensor maps carry the true width), the TMEM
+// residents are padded with zeros, so the score MMAs see zero-padded rows and
+// the accumulator columns >= p.dv stay zero and are never stored.
 template <class Op, bool CAUSAL, bool RAGGED>
 __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant__ typename Op::Params p) {
   static_assert(Op::NSB == 0 || Op::NSB == Op::NSA, "ring B stages pair with ring A stages");
@@ -375,18 +381,20 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
     typename Op::Row row;
     if constexpr (Op::TRES > 0) {
       // resident rows -> TMEM: warpgroup g copies residents g, g + 2, ...
-      // (rows at or beyond N are zeros)
+      // (rows at or beyond N, and columns at or beyond the head size p.dv
+      // of a narrower head, are zeros)
       const bool row_ok = blk0 + r < p.N;
       const size_t row_g = (size_t)head * p.N + (row_ok ? blk0 + r : 0);
+      const int dv8 = p.dv / 8;
       for (int s = g; s < Op::TRES; s += 2) {
-        const uint4* src = reinterpret_cast<const uint4*>(Op::tres_src(p, s)) + row_g * (Op::D / 8);
+        const uint4* src = reinterpret_cast<const uint4*>(Op::tres_src(p, s)) + row_g * dv8;
         const uint32_t col = tb + lane + Op::TRES_COL + (uint32_t)(s * (Op::D / 2));
 #pragma unroll
         for (int c = 0; c < Op::D / 32; ++c) {  // 16 columns = 32 bf16 per store
           uint32_t w[16];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const uint4 u = row_ok ? src[4 * c + q] : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 u = (row_ok && 4 * c + q < dv8) ? src[4 * c + q] : make_uint4(0u, 0u, 0u, 0u);
             w[4 * q] = u.x;
             w[4 * q + 1] = u.y;
             w[4 * q + 2] = u.z;

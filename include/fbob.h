@@ -32,7 +32,9 @@
  *   fp32.
  * - Every pointer must be 16-byte aligned and tensors must not overlap an
  *   output of the same call.
- * - Supported: d in {64, 128}; any N >= 1 (bf16 and fp32); causal or not.
+ * - Supported: d in {32, 64, 96, 128}; any N >= 1 (bf16 and fp32); causal or
+ *   not.  (bf16 heads of 32 and 96 run on the 64- and 128-column tensor-core
+ *   kernels with the missing columns zero-padded on chip.)
  *   B*H*N == 0 is a valid empty problem
  *   (returns FBOB_OK, launches nothing).
  * - Argument problems are reported BEFORE any launch (nothing is launched on

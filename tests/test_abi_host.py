@@ -73,7 +73,8 @@ def call_bob(lib, p, ptrs=None, ws=0x10000, ws_bytes=None):
 
 
 @pytest.mark.parametrize("field,value,status", [
-    ("d", 96, _lib.ERR_UNSUPPORTED),
+    ("d", 48, _lib.ERR_UNSUPPORTED),
+    ("d", 256, _lib.ERR_UNSUPPORTED),
     ("d", 0, _lib.ERR_INVALID_ARG),
     ("N", -1, _lib.ERR_INVALID_ARG),
     ("dtype", 7, _lib.ERR_INVALID_ARG),
