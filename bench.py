@@ -223,6 +223,10 @@ def run_ours(args, w):
         fb.attn_bob(x["Q"], x["K"], x["V"], O, x["dO"], L, D, x["UQ"], x["UK"], x["UV"], w.tau,
                     gQ, gK, gV, gdO, wsp, **cz)
 
+    def bob_four_pass():
+        fb.fbob_attn_bob_four_pass(x["Q"], x["K"], x["V"], O, x["dO"], L, D, x["UQ"], x["UK"], x["UV"], w.tau,
+                                   gQ, gK, gV, gdO, wsp, **cz)
+
     def barrier():
         if ws > 1:
             dist.barrier()
@@ -264,6 +268,17 @@ def run_ours(args, w):
     b1.record(stream)
     torch.cuda.synchronize()
     bob_ms = max_over_ranks(b0.elapsed_time(b1) / nb)
+
+    # ablation: the same BoB on the four-pass schedule (alpha, E, rows, columns)
+    for _ in range(2):
+        bob_four_pass()
+    b0.record(stream)
+    for _ in range(nb):
+        bob_four_pass()
+    b1.record(stream)
+    torch.cuda.synchronize()
+    four_ms = max_over_ranks(b0.elapsed_time(b1) / nb)
+    fb.device_status()
 
     # end to end through the public API from pinned host buffers
     out_host = [torch.empty(shp, dtype=torch.float32, pin_memory=True) for _ in range(4)]
@@ -315,6 +330,13 @@ def run_ours(args, w):
             "bob": {"ms_per_call": round(bob_ms, 4), "tflops": round(bob_tf, 3),
                     "frac_of_peak": round(bob_tf / pk, 4), "peak_tflops": pk, "peak_kind": pk_kind,
                     "counted_flops": flops_bob},
+            # the two-pass schedule against the four-pass one it collapses (same counted
+            # 38 N^2 d; the four-pass schedule executes 25 GEMMs per head, two-pass 20)
+            "ablation_four_pass": {"ms_per_call": round(four_ms, 4),
+                                   "tflops_counted": round(flops_bob / (four_ms * 1e-3) / 1e12, 3),
+                                   "two_pass_ms_per_call": round(bob_ms, 4),
+                                   "two_pass_speedup": round(four_ms / bob_ms, 3),
+                                   "gemms_executed_per_head": {"four_pass": 25, "two_pass": 20}},
             "e2e": {"value": round(job_tflops(ws, flops_step, e2e_ms), 3), "unit": "TFLOP/s",
                     "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             # our kernels launched in the timed region (per-kernel records of the library)

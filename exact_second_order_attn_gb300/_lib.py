@@ -24,7 +24,7 @@ FUNCTIONS = (
     "fbob_attn_fwd", "fbob_attn_bwd", "fbob_bob_workspace_bytes", "fbob_attn_bob",
     "fbob_device_status", "fbob_set_wait_limit_ns", "fbob_status_string", "fbob_last_error",
     "fbob_abi_version", "fbob_attn_bob_noalloc", "fbob_profile_enable", "fbob_profile_report",
-    "fbob_debug_stall_producer",
+    "fbob_debug_stall_producer", "fbob_attn_bob_four_pass",
 )
 
 
@@ -60,6 +60,8 @@ def load():
     lib.fbob_bob_workspace_bytes.restype = ctypes.c_size_t
     lib.fbob_attn_bob.argtypes = [cp] + [vp] * 15 + [ctypes.c_size_t, vp]
     lib.fbob_attn_bob.restype = st
+    lib.fbob_attn_bob_four_pass.argtypes = [cp] + [vp] * 15 + [ctypes.c_size_t, vp]
+    lib.fbob_attn_bob_four_pass.restype = st
     lib.fbob_attn_bob_noalloc.argtypes = [cp] + [vp] * 15
     lib.fbob_attn_bob_noalloc.restype = st
     lib.fbob_device_status.argtypes = [vp]
@@ -169,7 +171,7 @@ def fbob_bob_workspace_bytes(Q):
 
 
 def fbob_attn_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ=None, gK=None, gV=None, gdO=None,
-                  workspace=None, stream=None, causal=False):
+                  workspace=None, stream=None, causal=False, _entry="fbob_attn_bob"):
     """(gQ, gK, gV, gdO, workspace) = BoB; allocates outputs/workspace if not given.
 
     ``workspace`` is a float32 tensor [B, H, N, 2] holding (alpha, E) per row.
@@ -186,10 +188,18 @@ def fbob_attn_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ=None, gK=None, gV=No
     _same(Q, L, D, dtype=torch.float32, shape=Q.shape[:3])
     _same(Q, workspace, dtype=torch.float32)
     nbytes = workspace.numel() * 4
-    _check(load().fbob_attn_bob(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(D),
-                                _ptr(UQ), _ptr(UK), _ptr(UV), _ptr(gQ), _ptr(gK), _ptr(gV), _ptr(gdO),
-                                _ptr(workspace), ctypes.c_size_t(nbytes), _stream(stream)))
+    _check(getattr(load(), _entry)(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L),
+                                   _ptr(D), _ptr(UQ), _ptr(UK), _ptr(UV), _ptr(gQ), _ptr(gK), _ptr(gV), _ptr(gdO),
+                                   _ptr(workspace), ctypes.c_size_t(nbytes), _stream(stream)))
     return gQ, gK, gV, gdO, workspace
+
+
+def fbob_attn_bob_four_pass(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ=None, gK=None, gV=None, gdO=None,
+                            workspace=None, stream=None, causal=False):
+    """BoB on the four-pass schedule (the ablation of the two-pass one; bf16
+    only): same arguments and results as :func:`fbob_attn_bob`."""
+    return fbob_attn_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ, gK, gV, gdO, workspace, stream, causal,
+                         _entry="fbob_attn_bob_four_pass")
 
 
 def fbob_attn_bob_noalloc(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ=None, gK=None, gV=None, gdO=None,

@@ -165,6 +165,33 @@ fbob_status fbob_attn_bob(const fbob_problem* p, const void* Q, const void* K, c
   return FBOB_OK;
 }
 
+fbob_status fbob_attn_bob_four_pass(const fbob_problem* p, const void* Q, const void* K, const void* V,
+                                    const float* O, const void* dO, const float* L, const float* D, const void* UQ,
+                                    const void* UK, const void* UV, float* gQ, float* gK, float* gV, float* gdO,
+                                    float* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  bool empty = false;
+  fbob_status st = check_problem(p, &empty);
+  if (st != FBOB_OK) return st;
+  if (p->dtype != FBOB_BF16)
+    return fail(FBOB_ERR_UNSUPPORTED, "fbob_attn_bob_four_pass: the ablation schedule runs bf16 inputs only");
+  if (empty) return FBOB_OK;
+  const Ptr ps[] = {{Q, "Q"},   {K, "K"},   {V, "V"},   {O, "O"},   {dO, "dO"}, {L, "L"},    {D, "D"},
+                    {UQ, "UQ"}, {UK, "UK"}, {UV, "UV"}, {gQ, "gQ"}, {gK, "gK"}, {gV, "gV"}, {gdO, "gdO"}};
+  if ((st = check_ptrs(ps, 14)) != FBOB_OK) return st;
+  if (!workspace) return fail(FBOB_ERR_WORKSPACE, "workspace pointer is null");
+  if (!aligned16(workspace)) return fail(FBOB_ERR_WORKSPACE, "workspace is not 16-byte aligned");
+  const size_t need = fbob_bob_workspace_bytes(p);
+  if (workspace_bytes < need)
+    return fail(FBOB_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
+  fbob::DevCtx c;
+  if ((st = make_ctx(&c)) != FBOB_OK) return st;
+  fbob::BobArgs a{Q, K, V, dO, UQ, UK, UV, O, L, D, gQ, gK, gV, gdO, workspace, p->B * p->H, p->N, p->d, p->tau,
+                  p->causal != 0};
+  cudaError_t e = fbob::tc_bob_four_pass(a, c, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bob_four_pass launch");
+  return FBOB_OK;
+}
+
 fbob_status fbob_attn_bob_noalloc(const fbob_problem* p, const void* Q, const void* K, const void* V,
                                   const float* O, const void* dO, const float* L, const float* D, const void* UQ,
                                   const void* UK, const void* UV, float* gQ, float* gK, float* gV, float* gdO,

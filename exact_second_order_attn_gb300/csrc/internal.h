@@ -54,10 +54,11 @@ cudaError_t simt_fwd(const FwdArgs& a, const DevCtx& c, cudaStream_t s);
 cudaError_t simt_bwd(const BwdArgs& a, const DevCtx& c, cudaStream_t s);
 cudaError_t simt_bob(const BobArgs& a, const DevCtx& c, cudaStream_t s);
 
-// tc_fwd.cu / tc_bwd.cu / tc_bob.cu: tcgen05 kernels for bf16 inputs (N % 128 == 0).
+// tc_fwd.cu / tc_bwd.cu / tc_bob.cu: tcgen05 kernels for bf16 inputs (any N).
 cudaError_t tc_fwd(const FwdArgs& a, const DevCtx& c, cudaStream_t s);
 cudaError_t tc_bwd(const BwdArgs& a, const DevCtx& c, cudaStream_t s);
 cudaError_t tc_bob(const BobArgs& a, const DevCtx& c, cudaStream_t s);
+cudaError_t tc_bob_four_pass(const BobArgs& a, const DevCtx& c, cudaStream_t s);  // ablation schedule
 
 // bob_static.cu: the fixed (alpha, E) workspace of fbob_attn_bob_noalloc.
 size_t static_workspace_rows();           // capacity in query rows (B*H*N)

@@ -56,6 +56,7 @@ using namespace tile;
 struct P1Params {
   CUtensorMap mK, mUK, mV, mUV;              // streamed, box {64, 32} (U1-and-Y sweep)
   CUtensorMap mK64, mV64;                    // streamed, box {64, 64} (Z sweep)
+  CUtensorMap mUK64;                         // streamed, box {64, 64} (four-pass alpha sweep only)
   CUtensorMap mdO_res;                       // resident, box {64, 128} (U1-and-Y sweep at d = 128)
   const __nv_bfloat16 *Q, *UQ, *dO;          // resident (copied into TMEM)
   const float *L, *D, *O;
@@ -102,7 +103,13 @@ __device__ __forceinline__ void load_tile2(const CUtensorMap* m0, const CUtensor
 // Q and UQ sit in TMEM and dO in shared memory, with one score buffer whose
 // columns the two warpgroups split; at d = 64 Q, UQ, dO sit in TMEM with two
 // score buffers.
-template <int D_>
+//
+// DIRECT (the four-pass ablation's row-output sweep): alpha and E are known
+// from the two reduction sweeps before it, so the second operand is the full
+// cotangent of S, Sbar = P (Pbar - En) with Pbar = tau B (dP - D) + C - alpha dP
+// and En = sum_j P Pbar, and the kernel writes gQ = tau (dS UK + Sbar K)
+// summed over all keys - no row totals, no correction sweep.
+template <int D_, bool DIRECT = false>
 struct PassU1Y {
   using Params = P1Params;
   static constexpr int D = D_, DC = D / 64, T = 32;
@@ -113,7 +120,7 @@ struct PassU1Y {
   static constexpr int ACH = 4 * kBlk;                  // [K | UK | V | UV] per 64-column chunk
   static constexpr int SA = DC * ACH, SA_TX = SA, SB = 0, SB_TX = 0;
   static constexpr int NSA = kWide ? 4 : 8, NSB = 0;
-  static constexpr bool VEC = false, ROW_SUMS = true, TS = false;
+  static constexpr bool VEC = false, ROW_SUMS = !DIRECT, TS = false;
   static constexpr int VEC_OFF = 0, NVEC = 0, VEC_SCRATCH = 0;
   static constexpr int OPS = 4 * kChunk;                // dS, X, P, PB tiles; half h = columns 32h..32h+31
   static constexpr int ACC = 2 * D;                     // U1 | Y
@@ -168,15 +175,21 @@ struct PassU1Y {
     }
   }
   struct Row {
-    float nL, Di, alpha, ex;
+    float nL, Di, alpha, ex;   // DIRECT: alpha and ex = En are read, not summed
   };
   __device__ static void ew_init(Row& w, const Params& p, int blk0, int r, int head) {
     const bool ok = blk0 + r < p.N;   // ragged N: rows past the end are never stored
     const size_t vo = (size_t)head * p.N + (ok ? blk0 + r : 0);
     w.nL = ok ? -p.L[vo] * kLog2e : 0.f;
     w.Di = ok ? p.D[vo] : 0.f;
-    w.alpha = 0.f;
-    w.ex = 0.f;
+    if (DIRECT && ok) {
+      // the workspace holds (alpha, E) with E = sum_j P (C + tau B dP) = En + 2 alpha D
+      w.alpha = p.ws[2 * vo];
+      w.ex = fmaf(-2.f * w.alpha, w.Di, p.ws[2 * vo + 1]);
+    } else {
+      w.alpha = 0.f;
+      w.ex = 0.f;
+    }
   }
   // Operands are written 16 columns at a time.  With two score buffers the
   // operand half is acquired first (as in the dK/dV kernel); with one (split
@@ -206,10 +219,15 @@ struct PassU1Y {
           const float te = dP[j + e] - w.Di;
           pv[e] = pe;
           pb[e] = pe * be;
-          w.alpha += pb[e];
           ds[e] = pe * te;
-          x[e] = pe * fmaf(be, te, C[j + e]);
-          w.ex += x[e];
+          if (DIRECT) {
+            // Sbar = P (tau B (dP - D) + C - alpha dP - En)
+            x[e] = pe * (fmaf(be, te, C[j + e]) - fmaf(w.alpha, dP[j + e], w.ex));
+          } else {
+            w.alpha += pb[e];
+            x[e] = pe * fmaf(be, te, C[j + e]);
+            w.ex += x[e];
+          }
         }
         wdS[j / 2] = pack_bf16x2(ds[0], ds[1]);
         wX[j / 2] = pack_bf16x2(x[0], x[1]);
@@ -228,7 +246,7 @@ struct PassU1Y {
   }
   __device__ static void epilogue(Row& w, const Params& p, const EpiArgs& e) {
     float alpha = w.alpha, ex = w.ex;
-    if (!e.sum_rows(alpha, ex)) return;
+    if (!DIRECT && !e.sum_rows(alpha, ex)) return;   // DIRECT: alpha was read whole
     // every lane runs the (warp-collective) TMEM loads; rows >= N touch no memory
     const bool keep = e.blk0 + e.r < p.N;
     const size_t vo = (size_t)e.head * p.N + (keep ? e.blk0 + e.r : 0);
@@ -239,7 +257,11 @@ struct PassU1Y {
       float u1[16], y[16], o[16];
       tmem_ld16x2(e.tm + A_U1 + c0, e.tm + A_Y + c0, u1, y);
       if (!keep) continue;
-      store16(p.gQ + ro + c0, u1);   // U1, finished by the Z sweep
+      if (DIRECT) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) u1[j] *= p.tau;   // gQ = tau (dS UK + Sbar K)
+      }
+      store16(p.gQ + ro + c0, u1);   // two-pass: U1, finished by the Z sweep
       const float4* src = reinterpret_cast<const float4*>(p.O + ro + c0);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -251,7 +273,7 @@ struct PassU1Y {
       }
       store16(p.gdO + ro + c0, o);
     }
-    if (keep && e.g == 0) {
+    if (!DIRECT && keep && e.g == 0) {
       p.ws[2 * vo] = alpha;
       p.ws[2 * vo + 1] = fmaf(w.Di, alpha, ex);
     }
@@ -371,6 +393,160 @@ struct PassZ {
       }
       store16(p.gQ + ro + c0, o);
     }
+  }
+};
+
+// ===========================================================================
+// four-pass ablation: the reduction sweeps
+// ===========================================================================
+// Without the affine structure, reverse mode needs the row scalars in order:
+// alpha first (the cotangent of D), then E, whose natural form uses alpha,
+// then the row outputs with both known (PassU1Y<D, true>), then the column
+// pass.  These two kernels are the first two sweeps; they only reduce, so
+// they issue score MMAs alone (the accumulator warp just passes the
+// operand barriers through).
+
+// alpha sweep (64 keys per tile): alpha = sum_j P tau B.  Ring A = [K | UK];
+// Q, UQ in TMEM.
+template <int D_>
+struct PassAlpha {
+  using Params = P1Params;
+  static constexpr bool SPLIT = false, ROWS = true;
+  static constexpr int D = D_, DC = D / 64, T = 64, BLK = T * 128;
+  static constexpr int RES = 0, TRES = 2;   // Q, UQ
+  static constexpr int ACH = 2 * BLK;       // [K | UK] per 64-column chunk
+  static constexpr int SA = DC * ACH, SA_TX = SA, SB = 0, SB_TX = 0;
+  static constexpr int NSA = D == 128 ? 6 : 8, NSB = 0;
+  static constexpr bool VEC = false, ROW_SUMS = true, TS = false;
+  static constexpr int VEC_OFF = 0, NVEC = 0, VEC_SCRATCH = 0, OPS = 0;
+  static constexpr int ACC = 0, SCOLS = 2 * T, NBUF = 2;   // [S | B]
+  static constexpr int OP_HALF = 0, OP_COL = ACC + NBUF * SCOLS, TRES_COL = OP_COL;
+  static constexpr int SMEM = NSA * SA;
+  static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
+  static_assert(SMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
+
+  __device__ static const void* tres_src(const Params& p, int s) { return s == 0 ? (const void*)p.Q : (const void*)p.UQ; }
+  __device__ static void load_res(const Params&, uint8_t*, uint64_t*, int, int) {}
+  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head, bool) {
+    load_tile2(&p.mK64, &p.mUK64, st, DC, ACH, BLK, bar, t * T, head);
+  }
+  __device__ static void load_b(const Params&, uint8_t*, uint64_t*, int, int) {}
+  __device__ static void fill_vec(const Params&, float*, int, int, int) {}
+  __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t, uint32_t sa, uint32_t) {
+    const uint32_t i128 = idesc_bf16(kM, 2 * T, false, false), i64 = idesc_bf16(kM, T, false, false);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k)  // [S | Q UK^T] = Q [K; UK]^T
+      mma_ts_w(sc, tres_a(tres, 0, D, k), kmaj(sa, ACH, 0, k), i128, k > 0);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k)  // B += UQ K^T
+      mma_ts_w(sc + T, tres_a(tres, 1, D, k), kmaj(sa, ACH, 0, k), i64, 1);
+  }
+  __device__ static void accum_mmas(uint32_t, uint32_t, uint32_t, uint32_t, bool) {}
+  struct Row {
+    float nL, alpha;
+  };
+  __device__ static void ew_init(Row& w, const Params& p, int blk0, int r, int head) {
+    w.nL = blk0 + r < p.N ? -p.L[(size_t)head * p.N + blk0 + r] * kLog2e : 0.f;
+    w.alpha = 0.f;
+  }
+  template <bool MASK>
+  __device__ static bool ew_tile(Row& w, const Params& p, const TileArgs& a, const TileSync& s, int) {
+    const float sc = p.tau * kLog2e;
+#pragma unroll
+    for (int q = 0; q < T / 16; ++q) {
+      float S[16], B[16];
+      tmem_ld16x2(a.sc + q * 16, a.sc + T + q * 16, S, B);
+      if (q == T / 16 - 1) s.release_scores();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int col = q * 16 + j;   // tile column (key)
+        const float pe = (!MASK || (col >= a.lo && col <= a.hi)) ? ex2(fmaf(S[j], sc, w.nL)) : 0.f;
+        w.alpha = fmaf(pe, p.tau * B[j], w.alpha);
+      }
+    }
+    // no operands: pass the operand barriers through to the accumulator warp
+    if (!s.acquire_ops()) return false;
+    s.publish_ops();
+    return true;
+  }
+  __device__ static void epilogue(Row& w, const Params& p, const EpiArgs& e) {
+    float alpha = w.alpha, unused = 0.f;
+    if (!e.sum_rows(alpha, unused)) return;
+    if (e.g == 0 && e.blk0 + e.r < p.N) p.ws[2 * ((size_t)e.head * p.N + e.blk0 + e.r)] = alpha;
+  }
+};
+
+// E sweep (32 keys per tile): En = sum_j P Pbar, Pbar = tau B (dP - D) + C -
+// alpha dP with alpha from the alpha sweep; stores E = En + 2 alpha D, the
+// form the column pass reads.  Same streamed tile, residents and score MMAs
+// as the U1-and-Y sweep, two score buffers, no accumulators.
+template <int D_>
+struct PassE {
+  using Params = P1Params;
+  using Scores = PassU1Y<D_>;
+  static constexpr bool SPLIT = false, ROWS = true;
+  static constexpr int D = D_, DC = D / 64, T = 32;
+  static constexpr int TRES = Scores::TRES, RES = Scores::RES, ACH = Scores::ACH;
+  static constexpr int SA = DC * ACH, SA_TX = SA, SB = 0, SB_TX = 0;
+  static constexpr int NSA = D == 128 ? 5 : 8, NSB = 0;
+  static constexpr bool VEC = false, ROW_SUMS = true, TS = false;
+  static constexpr int VEC_OFF = 0, NVEC = 0, VEC_SCRATCH = 0, OPS = 0;
+  static constexpr int ACC = 0, SCOLS = 128, NBUF = 2;   // [S|B|dP|C]
+  static constexpr int OP_HALF = 0, OP_COL = ACC + NBUF * SCOLS, TRES_COL = OP_COL;
+  static constexpr int SMEM = RES + NSA * SA;
+  static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
+  static_assert(SMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
+
+  __device__ static const void* tres_src(const Params& p, int s) { return Scores::tres_src(p, s); }
+  __device__ static void load_res(const Params& p, uint8_t* res, uint64_t* bar, int row0, int head) {
+    Scores::load_res(p, res, bar, row0, head);
+  }
+  __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head, bool w) {
+    Scores::load_a(p, st, bar, t, head, w);
+  }
+  __device__ static void load_b(const Params&, uint8_t*, uint64_t*, int, int) {}
+  __device__ static void fill_vec(const Params&, float*, int, int, int) {}
+  __device__ static void score_mmas(uint32_t sc, uint32_t tres, uint32_t res, uint32_t sa, uint32_t sb) {
+    Scores::score_mmas(sc, tres, res, sa, sb);
+  }
+  __device__ static void accum_mmas(uint32_t, uint32_t, uint32_t, uint32_t, bool) {}
+  struct Row {
+    float nL, Di, alpha, en;
+  };
+  __device__ static void ew_init(Row& w, const Params& p, int blk0, int r, int head) {
+    const bool ok = blk0 + r < p.N;
+    const size_t vo = (size_t)head * p.N + (ok ? blk0 + r : 0);
+    w.nL = ok ? -p.L[vo] * kLog2e : 0.f;
+    w.Di = ok ? p.D[vo] : 0.f;
+    w.alpha = ok ? p.ws[2 * vo] : 0.f;
+    w.en = 0.f;
+  }
+  template <bool MASK>
+  __device__ static bool ew_tile(Row& w, const Params& p, const TileArgs& a, const TileSync& s, int) {
+    const float sc = p.tau * kLog2e;
+#pragma unroll
+    for (int q = 0; q < T / 16; ++q) {
+      float S[16], B[16], dP[16], C[16];
+      const uint32_t c = a.sc + q * 16;
+      tmem_ld16x4(c, c + 32, c + 64, c + 96, S, B, dP, C);
+      if (q == T / 16 - 1) s.release_scores();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int col = q * 16 + j;   // tile column (key)
+        const float pe = (!MASK || (col >= a.lo && col <= a.hi)) ? ex2(fmaf(S[j], sc, w.nL)) : 0.f;
+        const float pbar = fmaf(p.tau * B[j], dP[j] - w.Di, C[j]) - w.alpha * dP[j];
+        w.en = fmaf(pe, pbar, w.en);
+      }
+    }
+    if (!s.acquire_ops()) return false;
+    s.publish_ops();
+    return true;
+  }
+  __device__ static void epilogue(Row& w, const Params& p, const EpiArgs& e) {
+    float en = w.en, unused = 0.f;
+    if (!e.sum_rows(en, unused)) return;
+    if (e.g == 0 && e.blk0 + e.r < p.N)
+      p.ws[2 * ((size_t)e.head * p.N + e.blk0 + e.r) + 1] = fmaf(2.f * w.alpha, w.Di, en);
   }
 };
 
@@ -580,15 +756,15 @@ cudaError_t launch(const char* name, const typename Op::Params& prm, dim3 grid, 
   return cudaGetLastError();
 }
 
-template <int D>
-cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
-  P1Params p1;
+// Pass-1 parameters (the row sweeps of either schedule).
+bool make_p1(P1Params& p1, const BobArgs& a, const DevCtx& c, bool four_pass) {
   const int BH = a.BH, N = a.N;
   bool ok = make_bf16_map(&p1.mK, a.K, BH, N, a.d, kT) && make_bf16_map(&p1.mUK, a.UK, BH, N, a.d, kT) &&
             make_bf16_map(&p1.mV, a.V, BH, N, a.d, kT) && make_bf16_map(&p1.mUV, a.UV, BH, N, a.d, kT) &&
             make_bf16_map(&p1.mK64, a.K, BH, N, a.d, 64) && make_bf16_map(&p1.mV64, a.V, BH, N, a.d, 64) &&
             make_bf16_map(&p1.mdO_res, a.dO, BH, N, a.d, kM);
-  if (!ok) return cudaErrorInvalidValue;
+  if (four_pass) ok = ok && make_bf16_map(&p1.mUK64, a.UK, BH, N, a.d, 64);
+  if (!ok) return false;
   p1.Q = static_cast<const __nv_bfloat16*>(a.Q);
   p1.UQ = static_cast<const __nv_bfloat16*>(a.UQ);
   p1.dO = static_cast<const __nv_bfloat16*>(a.dO);
@@ -605,15 +781,17 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   p1.err = c.err;
   p1.wait_ns = c.wait_ns;
   p1.stall = c.stall;
-  const dim3 grid((N + kM - 1) / kM, BH);
-  // the Z kernel reads what the U1-and-Y kernel wrote (U1 in gQ, alpha and E)
-  cudaError_t e = launch<PassU1Y<D>>("bob_pass1_u1y", p1, grid, s);
-  if (e == cudaSuccess) e = launch<PassZ<D>>("bob_pass1_z", p1, grid, s);
-  if (e != cudaSuccess) return e;
+  return true;
+}
+
+// Pass 2 (the column pass, shared by both schedules): reads (alpha, E).
+template <int D>
+cudaError_t pass2_d(const BobArgs& a, const DevCtx& c, const dim3& grid, cudaStream_t s) {
+  const int BH = a.BH, N = a.N;
   P2Params p2;
-  ok = make_bf16_map(&p2.mQ, a.Q, BH, N, a.d, kT) && make_bf16_map(&p2.mUQ, a.UQ, BH, N, a.d, kT) &&
-       make_bf16_map(&p2.mdO, a.dO, BH, N, a.d, kT) && make_bf16_map(&p2.mV, a.V, BH, N, a.d, kM) &&
-       make_bf16_map(&p2.mUV, a.UV, BH, N, a.d, kM);
+  const bool ok = make_bf16_map(&p2.mQ, a.Q, BH, N, a.d, kT) && make_bf16_map(&p2.mUQ, a.UQ, BH, N, a.d, kT) &&
+                  make_bf16_map(&p2.mdO, a.dO, BH, N, a.d, kT) && make_bf16_map(&p2.mV, a.V, BH, N, a.d, kM) &&
+                  make_bf16_map(&p2.mUV, a.UV, BH, N, a.d, kM);
   if (!ok) return cudaErrorInvalidValue;
   p2.K = static_cast<const __nv_bfloat16*>(a.K);
   p2.UK = static_cast<const __nv_bfloat16*>(a.UK);
@@ -634,11 +812,40 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   return launch<Pass2<D>>("bob_pass2", p2, grid, s);
 }
 
+template <int D>
+cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
+  P1Params p1;
+  if (!make_p1(p1, a, c, false)) return cudaErrorInvalidValue;
+  const dim3 grid((a.N + kM - 1) / kM, a.BH);
+  // the Z kernel reads what the U1-and-Y kernel wrote (U1 in gQ, alpha and E)
+  cudaError_t e = launch<PassU1Y<D>>("bob_pass1_u1y", p1, grid, s);
+  if (e == cudaSuccess) e = launch<PassZ<D>>("bob_pass1_z", p1, grid, s);
+  if (e != cudaSuccess) return e;
+  return pass2_d<D>(a, c, grid, s);
+}
+
+// The four-pass schedule: alpha sweep, E sweep, row-output sweep, column pass.
+template <int D>
+cudaError_t bob4_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
+  P1Params p1;
+  if (!make_p1(p1, a, c, true)) return cudaErrorInvalidValue;
+  const dim3 grid((a.N + kM - 1) / kM, a.BH);
+  cudaError_t e = launch<PassAlpha<D>>("bob4_alpha", p1, grid, s);
+  if (e == cudaSuccess) e = launch<PassE<D>>("bob4_e", p1, grid, s);
+  if (e == cudaSuccess) e = launch<PassU1Y<D, true>>("bob4_rows", p1, grid, s);
+  if (e != cudaSuccess) return e;
+  return pass2_d<D>(a, c, grid, s);
+}
+
 }  // namespace
 
 cudaError_t tc_bob(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   // d = 32, 96 run on the d = 64, 128 kernels with zero-padded columns
   return a.d <= 64 ? bob_d<64>(a, c, s) : bob_d<128>(a, c, s);
+}
+
+cudaError_t tc_bob_four_pass(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
+  return a.d <= 64 ? bob4_d<64>(a, c, s) : bob4_d<128>(a, c, s);
 }
 
 }  // namespace fbob

@@ -136,6 +136,32 @@ fbob_status fbob_attn_bob(const fbob_problem* p,
                           cudaStream_t stream);
 
 /*
+ * BoB on the four-pass schedule, an ablation of the two-pass fbob_attn_bob
+ * ("FlashBoB", evolve.pub review - Strengths: the hierarchical affine
+ * structure collapses a natural four-pass schedule to two).  The pages name
+ * the four-pass schedule without spelling it out; this library's reading is
+ * the order plain reverse mode imposes when the row scalars are not split
+ * off affinely:
+ *   1. row sweep: alpha_i = sum_j P tau B;
+ *   2. row sweep: E in its natural form, which uses alpha (the cotangent of
+ *      P carries - alpha dP from D = rowsum(dO o O));
+ *   3. row sweep: gQ and gdO accumulated directly, alpha and E known;
+ *   4. column pass: gK, gV (the same kernel as fbob_attn_bob's pass 2).
+ * Same arguments, outputs (identical up to rounding order), workspace and
+ * errors as fbob_attn_bob; bf16 inputs only (fp32 returns
+ * FBOB_ERR_UNSUPPORTED).  It runs 25 GEMMs of 2 N^2 d per head against the
+ * two-pass schedule's 19 counted (20 executed).
+ */
+fbob_status fbob_attn_bob_four_pass(const fbob_problem* p,
+                                    const void* Q, const void* K, const void* V,
+                                    const float* O, const void* dO,
+                                    const float* L, const float* D,
+                                    const void* UQ, const void* UK, const void* UV,
+                                    float* gQ, float* gK, float* gV, float* gdO,
+                                    float* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream);
+
+/*
  * BoB without a caller workspace (the paper has no counterpart; this is a
  * convenience of this library).  Same inputs, outputs, passes and errors as
  * fbob_attn_bob, but the (alpha, E) workspace is a fixed device array inside

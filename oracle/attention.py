@@ -71,6 +71,8 @@ __all__ = [
     "attn_bwd",
     "attn_bob",
     "bob_row_scalars",
+    "bob_four_pass_rows",
+    "attn_bob_four_pass",
 ]
 
 # Largest number of fp64 score elements one row block materialises
@@ -230,6 +232,52 @@ def row_scalars(Qr, K, V, dOr, UQr, UK, UV, tau, qidx=None):
     return alpha, E
 
 
+def bob_four_pass_rows(Qr, K, V, dOr, UQr, UK, UV, tau, qidx=None):
+    """BoB of one query-row block computed in the order of the four-pass
+    schedule that the affine structure collapses to two (evolve.pub review,
+    Strengths: "collapsing a natural four-pass schedule to two").  The pages
+    do not spell the four passes out; the reading used here is the order
+    plain reverse mode forces when the row scalars are not split off:
+
+      1. alpha_i = sum_j P_ij B_ij (minus the adjoint of D);
+      2. En_i = sum_j P_ij Pbar_ij, the centre of the softmax reverse step,
+         where Pbar = C + B o (dP - D) - alpha dP needs alpha (the adjoint of
+         D reaches P through O = P V);
+      3. the row outputs with alpha and En known:
+         gQ = tau (dS UK + Sbar K), gdO = P UV + (P o B) V - alpha O,
+         Sbar = P o (Pbar - En);
+      4. the key-side outputs: gK = tau (dS^T UQ + Sbar^T Q),
+         gV = (P o (B - alpha))^T dO.
+
+    B = tau (UQ K^T + Q UK^T) and C = dO UV^T are the adjoints reaching dS
+    and (through dV) P, as in ``row_scalars``.  Returns
+    (gQ_rows, gK_part, gV_part, gdO_rows, alpha, En).
+    """
+    Qr, K, V, dOr = _f64(Qr), _f64(K), _f64(V), _f64(dOr)
+    UQr, UK, UV = _f64(UQr), _f64(UK), _f64(UV)
+    S = _mask(tau * (Qr @ K.T), qidx)
+    P, _ = _softmax_rows(S)
+    O = P @ V
+    dP = dOr @ V.T
+    D = (dOr * O).sum(axis=1)
+    B = tau * (UQr @ K.T + Qr @ UK.T)
+    C = dOr @ UV.T
+    # pass 1
+    alpha = (P * B).sum(axis=1)
+    # pass 2
+    P_bar = C + B * (dP - D[:, None]) - alpha[:, None] * dP
+    En = (P * P_bar).sum(axis=1)
+    # pass 3
+    dS = P * (dP - D[:, None])
+    S_bar = P * (P_bar - En[:, None])
+    gQ = tau * (dS @ UK + S_bar @ K)
+    gdO = P @ UV + (P * B) @ V - alpha[:, None] * O
+    # pass 4
+    gK = tau * (dS.T @ UQr + S_bar.T @ Qr)
+    gV = (P * (B - alpha[:, None])).T @ dOr
+    return gQ, gK, gV, gdO, alpha, En
+
+
 # ---------------------------------------------------------------------------
 # batched drivers over [..., N, d] arrays
 # ---------------------------------------------------------------------------
@@ -325,6 +373,36 @@ def bob_row_scalars(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
             alpha[h, rows], E[h, rows] = row_scalars(
                 Qh[h, rows], Kh[h], Vh[h], dOh[h, rows], UQh[h, rows], UKh[h], UVh[h], tau, _qidx(rows, causal))
     return alpha.reshape(lead + alpha.shape[1:]), E.reshape(lead + E.shape[1:])
+
+
+def attn_bob_four_pass(Q, K, V, dO, UQ, UK, UV, tau, causal=False):
+    """(gQ, gK, gV, gdO, alpha, En) for every head, in the four-pass order
+    (see ``bob_four_pass_rows``)."""
+    Qh, lead = _heads(Q)
+    Kh, _ = _heads(K)
+    Vh, _ = _heads(V)
+    dOh, _ = _heads(dO)
+    UQh, _ = _heads(UQ)
+    UKh, _ = _heads(UK)
+    UVh, _ = _heads(UV)
+    gQ = np.empty_like(Qh)
+    gK = np.zeros_like(Kh)
+    gV = np.zeros_like(Vh)
+    gdO = np.empty_like(dOh)
+    alpha = np.empty(Qh.shape[:-1])
+    En = np.empty(Qh.shape[:-1])
+    for h in range(Qh.shape[0]):
+        for rows in _row_blocks(Qh.shape[1]):
+            q, k, v, o, a, e = bob_four_pass_rows(Qh[h, rows], Kh[h], Vh[h], dOh[h, rows],
+                                                  UQh[h, rows], UKh[h], UVh[h], tau, _qidx(rows, causal))
+            gQ[h, rows] = q
+            gK[h] += k
+            gV[h] += v
+            gdO[h, rows] = o
+            alpha[h, rows] = a
+            En[h, rows] = e
+    shp = lambda a: a.reshape(lead + a.shape[1:])
+    return shp(gQ), shp(gK), shp(gV), shp(gdO), shp(alpha), shp(En)
 
 
 def bob_sampled_rows(Q, K, V, dO, UQ, UK, UV, tau, rows, causal=False):

@@ -154,3 +154,19 @@ def test_profile_report_empty_and_toggles(lib):
 def test_stall_hook_toggles_and_defaults_off(lib):
     assert lib.fbob_debug_stall_producer(1) == 0
     assert lib.fbob_debug_stall_producer(0) == 1
+
+
+def test_four_pass_validates_like_two_pass_and_refuses_fp32(lib):
+    """The ablation entry point checks its arguments before any launch, like
+    fbob_attn_bob, and runs bf16 inputs only."""
+    ptrs = [fake(0x1000 * (k + 1)) for k in range(14)]
+
+    def call(p, ws_bytes=None):
+        nb = lib.fbob_bob_workspace_bytes(ctypes.byref(p)) if ws_bytes is None else ws_bytes
+        return lib.fbob_attn_bob_four_pass(ctypes.byref(p), *ptrs, fake(0x10000), ctypes.c_size_t(nb), None)
+
+    assert call(_lib.Problem(1, 1, 256, 64, 0.125, _lib.FP32, 0)) == _lib.ERR_UNSUPPORTED
+    assert "bf16" in lib.fbob_last_error().decode()
+    assert call(_lib.Problem(1, 1, 256, 48, 0.125, _lib.BF16, 0)) == _lib.ERR_UNSUPPORTED
+    assert call(_lib.Problem(1, 1, 256, 64, 0.125, _lib.BF16, 0), ws_bytes=8) == _lib.ERR_WORKSPACE
+    assert call(_lib.Problem(1, 0, 256, 64, 0.125, _lib.BF16, 0)) == _lib.OK
