@@ -12,10 +12,11 @@ pass 2 recomputes each tile with the final alpha, E,
 (evolve.pub review, Summary and Key claims: two row scalars alpha, E, two
 passes; Strengths: alpha-free accumulators corrected after the reduction.)
 
-The tensor-core pass 1 runs as three sweeps over the same row blocks (TMEM
-holds one accumulator set at a time): U1 with alpha and E; then, with EX =
-E - D alpha read back, Z = sum_j (EX P + alpha dS) K_j and gQ = tau (U1 - Z);
-and Y with its own alpha.  `three_sweep_pass1` restates that order.
+The tensor-core pass 1 runs as two sweeps over the same row blocks (TMEM
+holds one kernel's accumulators): U1 and Y with alpha and E, writing
+gdO = Y - alpha O; then, with EX = E - D alpha read back,
+Z = sum_j (EX P + alpha dS) K_j and gQ = tau (U1 - Z).  `two_sweep_pass1`
+restates that order.
 """
 
 import numpy as np
@@ -65,7 +66,7 @@ def two_pass(Q, K, V, dO, UQ, UK, UV, tau, L, O, D, br=16, bc=8):
     return gQ, gK, gV, gdO, alpha, E
 
 
-def three_sweep_pass1(Q, K, V, dO, UQ, UK, UV, tau, L, O, D, br=16, bc=8):
+def two_sweep_pass1(Q, K, V, dO, UQ, UK, UV, tau, L, O, D, br=16, bc=8):
     N, d = Q.shape
     gQ, gdO = np.zeros_like(Q), np.zeros_like(Q)
     ws = np.zeros((N, 2))                           # (alpha, E) per row
@@ -75,16 +76,20 @@ def three_sweep_pass1(Q, K, V, dO, UQ, UK, UV, tau, L, O, D, br=16, bc=8):
             c = slice(j0, min(N, j0 + bc))
             yield c, np.exp(tau * Q[r] @ K[c].T - L[r, None])
 
-    for i0 in range(0, N, br):                      # sweep 1: U1, alpha, E
+    for i0 in range(0, N, br):                      # sweep 1: U1, Y, alpha, E; gdO = Y - alpha O
         r = slice(i0, min(N, i0 + br))
-        U1 = np.zeros((r.stop - r.start, d)); a = np.zeros(r.stop - r.start); ex = np.zeros_like(a)
+        n = r.stop - r.start
+        U1, Y = np.zeros((n, d)), np.zeros((n, d))
+        a, ex = np.zeros(n), np.zeros(n)
         for c, P in tiles(r):
             B = tau * (UQ[r] @ K[c].T + Q[r] @ UK[c].T)
             t = dO[r] @ V[c].T - D[r, None]
             X = P * (dO[r] @ UV[c].T + B * t)
             a += (P * B).sum(1); ex += X.sum(1)
             U1 += (P * t) @ UK[c] + X @ K[c]
+            Y += P @ UV[c] + (P * B) @ V[c]
         gQ[r] = U1
+        gdO[r] = Y - a[:, None] * O[r]
         ws[r, 0], ws[r, 1] = a, ex + D[r] * a
     for i0 in range(0, N, br):                      # sweep 2: Z, gQ = tau (U1 - Z)
         r = slice(i0, min(N, i0 + br))
@@ -94,25 +99,17 @@ def three_sweep_pass1(Q, K, V, dO, UQ, UK, UV, tau, L, O, D, br=16, bc=8):
             dS = P * (dO[r] @ V[c].T - D[r, None])
             Z += (ex[:, None] * P + a[:, None] * dS) @ K[c]
         gQ[r] = tau * (gQ[r] - Z)
-    for i0 in range(0, N, br):                      # sweep 3: Y, gdO = Y - alpha O
-        r = slice(i0, min(N, i0 + br))
-        Y = np.zeros((r.stop - r.start, d)); a = np.zeros(r.stop - r.start)
-        for c, P in tiles(r):
-            PB = P * tau * (UQ[r] @ K[c].T + Q[r] @ UK[c].T)
-            a += PB.sum(1)
-            Y += P @ UV[c] + PB @ V[c]
-        gdO[r] = Y - a[:, None] * O[r]
     return gQ, gdO, ws[:, 0], ws[:, 1]
 
 
 @pytest.mark.parametrize("N,d,sig", [(40, 8, (1,) * 7), (33, 5, (4, 4, 1, 1, 1, 1, 1)), (64, 16, (1, 1, 1, .1, .1, .1, .1))])
-def test_three_sweep_pass1_matches_node_by_node_oracle(N, d, sig):
+def test_two_sweep_pass1_matches_node_by_node_oracle(N, d, sig):
     rng = np.random.default_rng(N * d + 1)
     Q, K, V, dO, UQ, UK, UV = [rng.standard_normal((N, d)) * s for s in sig]
     tau = 1.0 / np.sqrt(d)
     O, L = orc.attn_fwd_head(Q, K, V, tau)
     _, _, _, D = orc.attn_bwd_rows(Q, K, V, dO, tau)
-    gQ, gdO, alpha, E = three_sweep_pass1(Q, K, V, dO, UQ, UK, UV, tau, L, O, D)
+    gQ, gdO, alpha, E = two_sweep_pass1(Q, K, V, dO, UQ, UK, UV, tau, L, O, D)
     ref = orc.bob_rows(Q, K, V, dO, UQ, UK, UV, tau)
     np.testing.assert_allclose(gQ, ref[0], rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(gdO, ref[3], rtol=1e-10, atol=1e-12)
