@@ -341,6 +341,10 @@ def run_ours(args, w):
                     "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             # our kernels launched in the timed region (per-kernel records of the library)
             "gpu_launches": int(sum(v[0] for v in kernels.values())),
+            # no N x N tensor exists: the process's peak device allocation (inputs,
+            # outputs, workspace, all on the caller's side) beside one fp32 N x N score matrix
+            "memory": {"peak_allocated_bytes": int(torch.cuda.max_memory_allocated()),
+                       "one_nxn_fp32_bytes": 4 * w.N * w.N * heads},
             "clocks": clk,
         }
         line["kernels"] = {k: {"launches": v[0], "avg_ms": round(v[1] / v[0], 4)} for k, v in kernels.items()}
@@ -506,10 +510,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(attn_inputs.WORKLOADS))
-    ap.add_argument("--cpu-rows", type=int, default=2048,
-                    help="query rows of one head per reference-arm step (CPU oracle)")
-    ap.add_argument("--baseline-rows", type=int, default=8192,
-                    help="query rows of one head in the cpu_baseline sample")
+    ap.add_argument("--cpu-rows", type=int, default=None,
+                    help="query rows of one head per reference-arm step (CPU oracle); "
+                         "default 2048 * 16384 / N (a fixed amount of oracle work), at most N")
+    ap.add_argument("--baseline-rows", type=int, default=None,
+                    help="query rows of one head in the cpu_baseline sample; "
+                         "default 16384 * 16384 / N (about ten seconds of oracle work), at most N")
     ap.add_argument("--causal", action="store_true",
                     help="causal mask (query i attends to keys j <= i); counted FLOPs scale by (N+1)/(2N)")
     ap.add_argument("--once", action="store_true",
@@ -518,6 +524,11 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     w = attn_inputs.WORKLOADS[args.workload]
+    # the oracle's cost per query row grows with N: size its samples by work, not rows
+    if args.cpu_rows is None:
+        args.cpu_rows = min(w.N, max(64, 2048 * 16384 // w.N))
+    if args.baseline_rows is None:
+        args.baseline_rows = min(w.N, max(128, 16384 * 16384 // w.N))
     if args.impl == "reference":
         run_reference(args, w)
     elif args.once:
