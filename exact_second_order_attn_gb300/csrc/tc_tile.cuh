@@ -361,6 +361,16 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
       bool ok = true;
       for (int t = 0; ok && t < nt; ++t) {
         ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.o_full[t & 1], (t >> 1) & 1, wt));
+        // With one score buffer read by one warpgroup per tile, S(t+2) waits
+        // for that warpgroup to have read S(t+1), a turnaround during which
+        // the tensor pipe has nothing queued; A(t), issued as soon as its
+        // operands exist, would instead run interleaved with S(t+1).  So A(t)
+        // waits for S(t+1) to complete and fills that turnaround.  (With
+        // split columns the buffer is released soon enough that A(t) would
+        // only delay S(t+2).  The barrier cannot run two phases ahead of this
+        // wait: that needs S(t+3) to complete, two score batches later.)
+        if (Op::NBUF == 1 && !Op::SPLIT && t + 1 < nt)
+          ok = ok && __all_sync(0xffffffffu, mbar_wait(&ctrl.s_full[(t + 1) & 1], ((t + 1) >> 1) & 1, wt));
         if (!ok) break;
         tc_fence_after();
         FBOB_STAMP(10, t);
