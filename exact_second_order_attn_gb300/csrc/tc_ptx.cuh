@@ -68,19 +68,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0u;
 }
 
-// Non-blocking probe of a phase (no suspend).
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0u;
-}
-
 // Two non-blocking probes in one instruction group: the second does not wait
 // for the first one's result, so the pair costs about one probe's latency.
 __device__ __forceinline__ bool mbar_test2(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1) {
@@ -95,11 +82,6 @@ __device__ __forceinline__ bool mbar_test2(uint64_t* b0, uint32_t p0, uint64_t* 
       : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1)
       : "memory");
   return ok != 0u;
-}
-
-// Warp-uniform probe: lane 0's view, broadcast to the warp.
-__device__ __forceinline__ bool mbar_test_w(uint64_t* bar, uint32_t parity) {
-  return __shfl_sync(0xffffffffu, (int)mbar_test(bar, parity), 0) != 0;
 }
 
 // Give-up state of one CTA: a shared abort flag that every role polls while
@@ -149,9 +131,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
-__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
 // Make generic-proxy shared-memory writes visible to the async proxy (MMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -160,6 +139,8 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // ---------------------------------------------------------------------------
 // TMEM
 // ---------------------------------------------------------------------------
+// A TMEM address holds the lane in bits 31..16 and the column in bits 15..0.
+// A warp may access only lanes 32 (warp % 4) .. 32 (warp % 4) + 31.
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
                "r"(ncols)
@@ -176,12 +157,6 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// TMEM address: lane in bits 31..16, column in bits 15..0.  Warp w of a
-// warpgroup may only touch lanes 32*(w%4) .. 32*(w%4)+31.
-__device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
-  return base + (lane << 16) + col;
 }
 
 // 16 consecutive fp32 columns of this thread's lane, waited for.
@@ -256,23 +231,6 @@ __device__ __forceinline__ void tmem_ld16x4(uint32_t a0, uint32_t a1, uint32_t a
   }
 }
 
-// Issue four 16-column loads of this thread's lane without waiting: r holds
-// garbage until tmem_wait_ld64(r).  The wait takes r as in/out operands, so
-// no use of r can be scheduled above it.
-__device__ __forceinline__ void tmem_ld16x4_issue(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%64];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%65];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47}, [%66];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%67];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld64(uint32_t* r) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63]) : : "memory");
-}
-
 // Store 16 consecutive 32-bit columns of this thread's lane (no wait).
 __device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t* r) {
   asm volatile(
@@ -287,15 +245,6 @@ __device__ __forceinline__ void tmem_st8_nowait(uint32_t taddr, const uint32_t* 
                : "memory");
 }
 
-// Store 8 consecutive 32-bit columns of this thread's lane and wait.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-      : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // tcgen05.mma, kind::f16 with bf16 operands and fp32 accumulation
 // ---------------------------------------------------------------------------
@@ -308,76 +257,21 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// Shared-memory operand descriptor with the 128-byte swizzle: start address,
-// leading / stride byte offsets (16-byte units), version 1 at bits 46-47,
-// swizzle mode 2 (128B) at bits 61-63.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
-  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]  (A K-major in TMEM: lane = row, each 32-bit
-// column holds two consecutive bf16 of K)
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // ---- fast issue: every shared-memory operand in this library uses the
 // 128-byte swizzle with SBO = 1024, so all descriptors share one high word;
 // only the low word (start address >> 4 | LBO >> 4 << 16) varies, and moving
-// along an operand adds (byte offset >> 4) to it.
+// along an operand adds (byte offset >> 4) to it.  High word: SBO >> 4 (bits
+// 32-45 of the descriptor), version 1 (bits 46-47), swizzle mode 2 = 128-byte
+// (bits 61-63).
 constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
 
 __host__ __device__ constexpr uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
   return (saddr >> 4) | ((lbo_bytes >> 4) << 16);
 }
 
-// D[tmem] (+)= A[smem] * B[smem], descriptors given by their low words.
-__device__ __forceinline__ void mma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
-      "mov.b64 ad, {%1, %5};\n\t"
-      "mov.b64 bd, {%2, %5};\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem], B descriptor given by its low word.
-__device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
-      "mov.b64 bd, {%2, %5};\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
-      : "memory");
-}
-
+// D[tmem] (+)= A * B with B from shared memory (descriptor low word) and A
+// from shared memory (mma_ss_w) or from TMEM (mma_ts_w: lane = row of A, each
+// 32-bit column two consecutive bf16 of K).
 // Warp-wide issue: the whole (converged) MMA warp executes these, elect.sync
 // picks lane 0 to issue.  Keeping the issuing code warp-uniform lets the
 // operands stay in uniform registers; a divergent single-thread issue costs
@@ -413,13 +307,6 @@ __device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
       : "memory");
 }
 
-// Arrive (once) on the mbarrier when all previously issued tcgen05 ops of
-// this thread have completed.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // operand writes from registers
 // ---------------------------------------------------------------------------
@@ -438,13 +325,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
 }
-
-// Named barrier over a subset of warps.
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-__device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31u) == 0u; }
 
 }  // namespace tc
 }  // namespace fbob

@@ -544,14 +544,6 @@ __device__ __forceinline__ void write_op_cols(uint32_t tile, uint32_t r, int col
                  w[4 * cc + 3]);
 }
 
-// Write 32 packed bf16 (16 words) of row r into columns [32h, 32h+32) of a
-// 128B-swizzled [128][64] operand tile.
-__device__ __forceinline__ void write_op_half(uint32_t tile, uint32_t r, uint32_t h, const uint32_t* w) {
-#pragma unroll
-  for (int cc = 0; cc < 4; ++cc)
-    st_shared_v4(tile + sw128_offset(r, 4 * h + cc), w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
-}
-
 __device__ __forceinline__ void store16(float* dst, const float* v) {
   float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
