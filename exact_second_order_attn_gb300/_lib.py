@@ -170,12 +170,8 @@ def fbob_bob_workspace_bytes(Q):
     return int(load().fbob_bob_workspace_bytes(ctypes.byref(p)))
 
 
-def fbob_attn_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ=None, gK=None, gV=None, gdO=None,
-                  workspace=None, stream=None, causal=False, _entry="fbob_attn_bob"):
-    """(gQ, gK, gV, gdO, workspace) = BoB; allocates outputs/workspace if not given.
-
-    ``workspace`` is a float32 tensor [B, H, N, 2] holding (alpha, E) per row.
-    """
+def _bob_call(entry, Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ, gK, gV, gdO, workspace, stream, causal):
+    """Marshal the arguments of one of the workspace-taking BoB entry points."""
     p = problem_for(Q, tau, causal)
     gQ = _empty(Q) if gQ is None else gQ
     gK = _empty(Q) if gK is None else gK
@@ -188,18 +184,28 @@ def fbob_attn_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ=None, gK=None, gV=No
     _same(Q, L, D, dtype=torch.float32, shape=Q.shape[:3])
     _same(Q, workspace, dtype=torch.float32)
     nbytes = workspace.numel() * 4
-    _check(getattr(load(), _entry)(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L),
-                                   _ptr(D), _ptr(UQ), _ptr(UK), _ptr(UV), _ptr(gQ), _ptr(gK), _ptr(gV), _ptr(gdO),
-                                   _ptr(workspace), ctypes.c_size_t(nbytes), _stream(stream)))
+    _check(getattr(load(), entry)(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(L), _ptr(D),
+                                  _ptr(UQ), _ptr(UK), _ptr(UV), _ptr(gQ), _ptr(gK), _ptr(gV), _ptr(gdO),
+                                  _ptr(workspace), ctypes.c_size_t(nbytes), _stream(stream)))
     return gQ, gK, gV, gdO, workspace
+
+
+def fbob_attn_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ=None, gK=None, gV=None, gdO=None,
+                  workspace=None, stream=None, causal=False):
+    """(gQ, gK, gV, gdO, workspace) = BoB; allocates outputs/workspace if not given.
+
+    ``workspace`` is a float32 tensor [B, H, N, 2] holding (alpha, E) per row.
+    """
+    return _bob_call("fbob_attn_bob", Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ, gK, gV, gdO, workspace,
+                     stream, causal)
 
 
 def fbob_attn_bob_four_pass(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ=None, gK=None, gV=None, gdO=None,
                             workspace=None, stream=None, causal=False):
     """BoB on the four-pass schedule (the ablation of the two-pass one; bf16
     only): same arguments and results as :func:`fbob_attn_bob`."""
-    return fbob_attn_bob(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ, gK, gV, gdO, workspace, stream, causal,
-                         _entry="fbob_attn_bob_four_pass")
+    return _bob_call("fbob_attn_bob_four_pass", Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ, gK, gV, gdO,
+                     workspace, stream, causal)
 
 
 def fbob_attn_bob_noalloc(Q, K, V, O, dO, L, D, UQ, UK, UV, tau, gQ=None, gK=None, gV=None, gdO=None,
