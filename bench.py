@@ -99,7 +99,8 @@ class _Nvml:
 class Clocks:
     """SM clock and throttle reasons sampled DURING the timed region: an NVML
     poller thread (every 2 ms, so short regions get samples too), else
-    nvidia-smi -lms 200.  Samples go to gpurun_out/clocks_rank<i>.csv."""
+    nvidia-smi -lms 200.  The samples are kept in clocks_rank<i>.csv beside the
+    run's other logs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
