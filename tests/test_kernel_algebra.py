@@ -16,7 +16,8 @@ The tensor-core pass 1 runs as two sweeps over the same row blocks (TMEM
 holds one kernel's accumulators): U1 and Y with alpha and E, writing
 gdO = Y - alpha O; then, with EX = E - D alpha read back,
 Z = sum_j (EX P + alpha dS) K_j and gQ = tau (U1 - Z).  `two_sweep_pass1`
-restates that order.
+restates that order; `four_pass_sweeps` restates the four-pass ablation's
+three row sweeps the same way.
 """
 
 import numpy as np
@@ -133,3 +134,68 @@ def test_two_pass_schedule_matches_node_by_node_oracle(N, d, sig):
     alpha, E = orc.row_scalars(Q, K, V, dO, UQ, UK, UV, tau)
     np.testing.assert_allclose(got[4], alpha, rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(got[5], E, rtol=1e-10, atol=1e-12)
+
+
+def four_pass_sweeps(Q, K, V, dO, UQ, UK, UV, tau, L, O, D, br=16, bc=8):
+    """The four-pass ablation's three row sweeps as the kernels compute them:
+    alpha; then E stored as En + 2 alpha D (En = sum_j P Pbar with Pbar =
+    tau B (dP - D) + C - alpha dP); then, with En = E - 2 alpha D read back,
+    gQ = tau sum_j (dS UK + Sbar K), Sbar = P (Pbar - En), and gdO = Y - alpha O."""
+    N, d = Q.shape
+    ws = np.zeros((N, 2))
+    gQ, gdO = np.zeros_like(Q), np.zeros_like(Q)
+
+    def tiles(r):
+        for j0 in range(0, N, bc):
+            c = slice(j0, min(N, j0 + bc))
+            yield c, np.exp(tau * Q[r] @ K[c].T - L[r, None])
+
+    for i0 in range(0, N, br):                      # sweep 1: alpha
+        r = slice(i0, min(N, i0 + br))
+        a = np.zeros(r.stop - r.start)
+        for c, P in tiles(r):
+            a += (P * tau * (UQ[r] @ K[c].T + Q[r] @ UK[c].T)).sum(1)
+        ws[r, 0] = a
+    for i0 in range(0, N, br):                      # sweep 2: E (natural form, needs alpha)
+        r = slice(i0, min(N, i0 + br))
+        a = ws[r, 0]
+        en = np.zeros(r.stop - r.start)
+        for c, P in tiles(r):
+            B = tau * (UQ[r] @ K[c].T + Q[r] @ UK[c].T)
+            dP = dO[r] @ V[c].T
+            en += (P * (B * (dP - D[r, None]) + dO[r] @ UV[c].T - a[:, None] * dP)).sum(1)
+        ws[r, 1] = en + 2 * a * D[r]
+    for i0 in range(0, N, br):                      # sweep 3: the row outputs, alpha and E known
+        r = slice(i0, min(N, i0 + br))
+        a = ws[r, 0]
+        en = ws[r, 1] - 2 * a * D[r]
+        n = r.stop - r.start
+        G, Y = np.zeros((n, d)), np.zeros((n, d))
+        for c, P in tiles(r):
+            B = tau * (UQ[r] @ K[c].T + Q[r] @ UK[c].T)
+            dP = dO[r] @ V[c].T
+            t = dP - D[r, None]
+            Sbar = P * (B * t + dO[r] @ UV[c].T - (a[:, None] * dP + en[:, None]))
+            G += (P * t) @ UK[c] + Sbar @ K[c]
+            Y += P @ UV[c] + (P * B) @ V[c]
+        gQ[r] = tau * G
+        gdO[r] = Y - a[:, None] * O[r]
+    return gQ, gdO, ws[:, 0], ws[:, 1]
+
+
+@pytest.mark.parametrize("N,d,sig", [(40, 8, (1,) * 7), (33, 5, (4, 4, 1, 1, 1, 1, 1)), (64, 16, (1, 1, 1, .1, .1, .1, .1))])
+def test_four_pass_sweeps_match_node_by_node_oracle(N, d, sig):
+    rng = np.random.default_rng(N * d + 3)
+    Q, K, V, dO, UQ, UK, UV = [rng.standard_normal((N, d)) * s for s in sig]
+    tau = 1.0 / np.sqrt(d)
+    O, L = orc.attn_fwd_head(Q, K, V, tau)
+    _, _, _, D = orc.attn_bwd_rows(Q, K, V, dO, tau)
+    gQ, gdO, alpha, E = four_pass_sweeps(Q, K, V, dO, UQ, UK, UV, tau, L, O, D)
+    ref = orc.bob_rows(Q, K, V, dO, UQ, UK, UV, tau)
+    # the direct sweep recovers En = E - 2 alpha D by a subtraction that cancels on
+    # peaky rows: compare at fp64 rounding of the tensor's scale, not of each element
+    np.testing.assert_allclose(gQ, ref[0], rtol=1e-10, atol=1e-10 * np.abs(ref[0]).max())
+    np.testing.assert_allclose(gdO, ref[3], rtol=1e-10, atol=1e-10 * np.abs(ref[3]).max())
+    ra, rE = orc.row_scalars(Q, K, V, dO, UQ, UK, UV, tau)
+    np.testing.assert_allclose(alpha, ra, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(E, rE, rtol=1e-10, atol=1e-12)   # the workspace form pass 2 reads
