@@ -172,9 +172,14 @@ fbob_status fbob_attn_bob_four_pass(const fbob_problem* p,
  *   - Capacity: B*H*N <= 2097152 (2^21) query rows; larger problems return
  *     FBOB_ERR_UNSUPPORTED before any launch.  Every GPU that loads the
  *     library holds the array (16 MiB) until the process exits.
- *   - The first call on a device looks up the array's device address with
- *     that device current (cudaGetSymbolAddress) and caches it; make that
- *     first call before any stream capture on the device.
+ *   - The array's device address belongs to the CUDA context the library's
+ *     device code is loaded into.  The first call in a context (per device:
+ *     its primary context, a non-primary context the caller made current, or
+ *     the new context after cudaDeviceReset) looks the address up with that
+ *     device current (cudaGetSymbolAddress, which may load the library's
+ *     device code) and saves it for later calls in the same context; make
+ *     that first call - on every device, and again after a cudaDeviceReset -
+ *     before any stream capture.
  *   - All calls on a device share the array: calls whose kernels overlap on
  *     the GPU (e.g. on two unordered streams) race and give wrong results.
  *     Calls ordered on one stream are safe; no clearing is needed between

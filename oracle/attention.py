@@ -33,7 +33,7 @@ Notation (per head, row-major, rows i = queries, rows j = keys):
         with respect to (Q, K, V, dO)  ->  (gQ, gK, gV, gdO)
         (the pages write these four outputs as ed(Q), ed(K), ed(V), ed(dO)).
 
-Readings where the pages are silent (each is also listed in the design doc):
+Readings where the pages are silent:
 * g is a function of (Q, K, V, dO) only; O is not an independent input, so
   D = rowsum(dO o O) is differentiated through O = P V.
 * tau multiplies the scores once: S = tau Q K^T.

@@ -29,6 +29,12 @@ def test_roofline_takes_the_dominant_kernel_and_scales_traffic_by_heads(tmp_path
     assert r["achieved"] == pytest.approx(flops / 17.5e-3 / 1e12, rel=1e-4)
     assert r["frac"] == pytest.approx(r["achieved"] / 1700.0, rel=1e-3)
     assert r["traffic"] == pytest.approx(344e6 * (w.B * w.H) / 8)
+    # pass 2 re-reads Q, UQ, dO (bf16) and L, D, alpha, E (fp32) once per key block of 128
+    N, d, h = w.N, w.d, w.B * w.H
+    assert r["ledger_bytes"] == pytest.approx(h * (16 * N * d + (6 * d + 16) * N * N / 128))
+    assert r["compulsory_bytes"] == pytest.approx(h * (22 * N * d + 16 * N))
+    assert r["traffic_over_ledger"] == pytest.approx(r["traffic"] / r["ledger_bytes"], abs=1e-4)
+    assert r["traffic_over_compulsory"] == pytest.approx(r["traffic"] / r["compulsory_bytes"], abs=1e-4)
 
 
 @pytest.mark.parametrize("why", ["stale_hash", "causal", "other_d", "other_kernel"])
@@ -63,7 +69,7 @@ class _FakeNvml:
 
 
 def test_clocks_nvml_record_is_median_and_union_of_reasons(tmp_path, monkeypatch):
-    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setenv("FBOB_CLOCK_DIR", str(tmp_path / "logs"))
     seq = [(2070.0, []), (1980.0, ["sw_power_cap"]), (2070.0, []), (2055.0, ["sw_power_cap"])]
     monkeypatch.setattr(bench, "_Nvml", lambda index: _FakeNvml(seq))
     c = bench.Clocks(0)
@@ -76,11 +82,11 @@ def test_clocks_nvml_record_is_median_and_union_of_reasons(tmp_path, monkeypatch
     assert rec["samples"] >= len(seq)
     assert rec["reasons"] == ["sw_power_cap"]
     assert 1980.0 <= rec["sm_mhz"] <= 2070.0
-    assert (tmp_path / "gpurun_out" / "clocks_rank0.csv").read_text().startswith("sm_mhz,sm_max_mhz,reasons")
+    assert (tmp_path / "logs" / "clocks_rank0.csv").read_text().startswith("sm_mhz,sm_max_mhz,reasons")
 
 
 def test_clocks_nvml_records_nothing_before_the_timed_region(tmp_path, monkeypatch):
-    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setenv("FBOB_CLOCK_DIR", str(tmp_path))
     monkeypatch.setattr(bench, "_Nvml", lambda index: _FakeNvml([(1000.0, ["hw_slowdown"])]))
     c = bench.Clocks(0)
     c.start()
@@ -101,7 +107,7 @@ class _FakeProc:
 
 
 def test_clocks_nvidia_smi_fallback_parses_reasons(tmp_path, monkeypatch):
-    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setenv("FBOB_CLOCK_DIR", str(tmp_path))
     c = bench.Clocks(0)
     os.makedirs(os.path.dirname(c.path), exist_ok=True)
     rows = ["0, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active",
@@ -114,3 +120,30 @@ def test_clocks_nvidia_smi_fallback_parses_reasons(tmp_path, monkeypatch):
     rec = c.stop()
     assert rec == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3,
                    "source": "nvidia-smi"}
+
+
+def test_bob_ledger_is_the_pages_formula_in_bytes_and_the_kernels_add_the_z_sweep(tmp_path, monkeypatch):
+    """Theorem 4.3's ledger (evolve.pub review, Strengths "Theory honestly
+    scoped"): 12Nd + 4N + 4dN^2/B_r + (3d+4)N^2/B_c words per head; here in
+    bytes with bf16 inputs (Q, K, V, dO, UQ, UK, UV) and fp32 O, vectors and
+    outputs.  The kernels as built add the Z sweep: K, V streamed once more
+    per row block, Q, dO, L, D, (alpha, E) read again and U1 round-tripped."""
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))   # no committed counters
+    w = attn_inputs.small(1, 1, 1024, 64, "bf16")
+    N, d = w.N, w.d
+    led = bench.bob_ledger(w)
+    words = {"Q dO UQ K V UK UV (bf16)": 7 * N * d * 2, "O (fp32)": N * d * 4, "outputs (fp32)": 4 * N * d * 4,
+             "L D in, alpha E out": 4 * N * 4, "pass 1 streams": 4 * d * N * N / 128 * 2,
+             "pass 2 streams": (3 * d * 2 + 4 * 4) * N * N / 128}
+    assert led["pages_ledger_bytes"] == pytest.approx(sum(words.values()))
+    z_sweep = 2 * d * N * N / 128 * 2 + (2 * N * d * 2 + 4 * N * 4) + 2 * N * d * 4
+    assert led["kernels_ledger_bytes"] == pytest.approx(led["pages_ledger_bytes"] + z_sweep)
+    assert led["measured_dram_bytes"] is None and "measured_over_ledger" not in led
+    assert led["compulsory_bytes"] < led["kernels_ledger_bytes"]
+
+
+def test_gpus_must_match_the_launched_ranks():
+    bench.check_gpus(1, 1)
+    bench.check_gpus(4, 4)
+    with pytest.raises(SystemExit):
+        bench.check_gpus(8, 1)
