@@ -59,6 +59,8 @@ cudaError_t tc_fwd(const FwdArgs& a, const DevCtx& c, cudaStream_t s);
 cudaError_t tc_bwd(const BwdArgs& a, const DevCtx& c, cudaStream_t s);
 cudaError_t tc_bob(const BobArgs& a, const DevCtx& c, cudaStream_t s);
 cudaError_t tc_bob_four_pass(const BobArgs& a, const DevCtx& c, cudaStream_t s);  // ablation schedule
+// tc_bob_cols.cu: BoB pass 2 (gK, gV) for heads of 65 to 128 columns.
+cudaError_t tc_bob_cols_wide(const BobArgs& a, const DevCtx& c, cudaStream_t s);
 
 // bob_static.cu: the fixed (alpha, E) workspace of fbob_attn_bob_noalloc.
 size_t static_workspace_rows();           // capacity in query rows (B*H*N)

@@ -821,7 +821,8 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   cudaError_t e = launch<PassU1Y<D>>("bob_pass1_u1y", p1, grid, s);
   if (e == cudaSuccess) e = launch<PassZ<D>>("bob_pass1_z", p1, grid, s);
   if (e != cudaSuccess) return e;
-  return pass2_d<D>(a, c, grid, s);
+  if constexpr (D == 128) return tc_bob_cols_wide(a, c, s);
+  else return pass2_d<D>(a, c, grid, s);
 }
 
 // The four-pass schedule: alpha sweep, E sweep, row-output sweep, column pass.
@@ -834,7 +835,8 @@ cudaError_t bob4_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   if (e == cudaSuccess) e = launch<PassE<D>>("bob4_e", p1, grid, s);
   if (e == cudaSuccess) e = launch<PassU1Y<D, true>>("bob4_rows", p1, grid, s);
   if (e != cudaSuccess) return e;
-  return pass2_d<D>(a, c, grid, s);
+  if constexpr (D == 128) return tc_bob_cols_wide(a, c, s);
+  else return pass2_d<D>(a, c, grid, s);
 }
 
 }  // namespace

@@ -8,13 +8,20 @@
 // in all at d = 128).  Per tile t and block X:
 //   S_X = Q_X K_t^T         one SS MMA of N = 128 (issued by warp 9);
 //   softmax (warpgroup X, thread r = row r): two passes over S_X - the row
-//     max, then P = 2^(x - m) with x = tau log2(e) S - written as bf16 over
-//     the first 64 columns of S_X;
-//   O_X += P V_t            TS MMA, P read from TMEM (issued by warp 10).
-// Because P overwrites S, S_X(t+1) is issued only after O_X += P V_t has
-// completed.  The running max moves only when a row's tile max exceeds it by
-// more than 8 (lazy rescale), so P <= 2^8 stays well inside bf16 and O_X is
-// rescaled in TMEM only then (after the previous P V product has landed).
+//     max, then P = 2^(x - m) with x = tau log2(e) S - written over S_X as
+//     two bf16 terms, P = P_hi + P_lo with P_hi = bf16(P) and P_lo =
+//     bf16(P - P_hi): each 32-column chunk of S holds the P_hi of its 32
+//     keys in its first 16 columns and their P_lo in the last 16;
+//   O_X += P_hi V_t + P_lo V_t   TS MMAs, P read from TMEM (issued by warp 10).
+// The split makes O exact to about 2^-17 relative instead of the 2^-9 of one
+// bf16 rounding of P.  That matters downstream: D = rowsum(dO o O) feeds
+// dP - D, which nearly cancels on the dominant key of a peaked softmax row,
+// so an O (and D) carrying P's rounding would spoil dQ, dK and every BoB
+// output there.  Because P overwrites S, S_X(t+1) is issued only after the
+// P V products of tile t have completed.  The running max moves only when a
+// row's tile max exceeds it by more than 8 (lazy rescale), so P <= 2^8 stays
+// well inside bf16 and O_X is rescaled in TMEM only then (after the previous
+// P V products have landed).
 // O = O_X / l, L = (m + log2 l) ln 2.  Warp 8 issues TMA.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -75,9 +82,10 @@ struct Ctrl {
 // One tile of the softmax of one row (this thread's TMEM lane): pass 1 finds
 // the tile's row max over columns 0..lim, a lazy rescale of O and l follows
 // when the max grew by more than 2^8 (after the block's previous P V product
-// has landed), pass 2 writes P = 2^(x - m) as bf16 over the first 64 columns
-// of S (chunk c writes columns 16c..16c+15, all already read) and sums it
-// into ls.  MASK = false skips the column test (tiles below the diagonal).
+// has landed), pass 2 writes P = 2^(x - m) as P_hi + P_lo over S (chunk c
+// reads columns 32c..32c+31 and writes P_hi into 32c..32c+15, P_lo into
+// 32c+16..32c+31) and sums P into ls.  MASK = false skips the column test
+// (tiles below the diagonal).
 template <int D, bool MASK>
 __device__ __forceinline__ bool softmax_tile(uint32_t s_col, uint32_t o_col, int lim, float sc, float& m, float& l,
                                              float& ls, uint64_t& o_done, int t, const Waiter& wt) {
@@ -115,15 +123,19 @@ __device__ __forceinline__ bool softmax_tile(uint32_t s_col, uint32_t o_col, int
   for (int c = 0; c < kKT / 32; ++c) {
     float s[32];
     tmem_ld32(s_col + 32 * c, s);
-    uint32_t w[16];
+    uint32_t wh[16], wl[16];
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
       const float p0 = (!MASK || 32 * c + j <= lim) ? tile::ex2(fmaf(s[j], sc, -m)) : 0.f;
       const float p1 = (!MASK || 32 * c + j + 1 <= lim) ? tile::ex2(fmaf(s[j + 1], sc, -m)) : 0.f;
       ls += p0 + p1;
-      w[j / 2] = pack_bf16x2(p0, p1);
+      const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+      const float2 hf = __bfloat1622float2(h);
+      wh[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
+      wl[j / 2] = pack_bf16x2(p0 - hf.x, p1 - hf.y);   // exact differences, rounded once more
     }
-    tmem_st16_nowait(s_col + 16 * c, w);
+    tmem_st16_nowait(s_col + 32 * c, wh);
+    tmem_st16_nowait(s_col + 32 * c + 16, wl);
   }
   return true;
 }
@@ -259,9 +271,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc(const __grid_constant
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kKT / 16; ++kk)
-            mma_ts_w(tb + x * D, tb + C::S_COL + x * kKT + kk * 8, tile::mnmaj(v_mn, 0, kk), id,
-                     (t > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kKT / 16; ++kk) {
+            // keys 16 kk .. 16 kk + 15: P_hi at column 32 (kk / 2) + 8 (kk % 2), P_lo 16 columns on
+            const uint32_t a = tb + C::S_COL + x * kKT + 32 * (kk >> 1) + 8 * (kk & 1);
+            mma_ts_w(tb + x * D, a, tile::mnmaj(v_mn, 0, kk), id, (t > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_w(tb + x * D, a + 16, tile::mnmaj(v_mn, 0, kk), id, 1u);
+          }
           mma_commit_w(&ctrl.o_done[x]);
         }
         if (ok) mma_commit_w(&ctrl.v_empty[sv]);
