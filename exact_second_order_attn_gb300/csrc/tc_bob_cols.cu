@@ -342,11 +342,12 @@ __global__ void __launch_bounds__(kThreads, 1) bob_cols_wide(const __grid_consta
     }
   } else if (warp == kAccWarp) {
     // --------------------------------------------------- accumulator MMAs
-    // gV(t) as soon as Gdp(t) is written (after phase A of tile t was read),
-    // gK(t) as soon as dS(t), Gs(t) are (after phase B).  The dO stage is
-    // released by gV(t) together with B(t) (other warp), the [Q | UQ] stage
-    // by gK(t), which needs phase B's operands and so follows every other
-    // reader of the stage.
+    // gV(t) as soon as Gdp(t) is written (after phase A of tile t was read)
+    // and tile t's dO has landed - phase A does not read dO, so Gdp(t) can
+    // exist before it; gK(t) as soon as dS(t), Gs(t) are (after phase B).
+    // The dO stage is released by gV(t) together with B(t) (other warp), the
+    // [Q | UQ] stage by gK(t), which needs phase B's operands and so follows
+    // every other reader of the stage.
     if (live) {
       const uint32_t id = idesc_bf16(kM, kD, false, true);
       const uint32_t ops_l = desc_lo(sm0 + kOPS_OFF, 16);
@@ -354,6 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) bob_cols_wide(const __grid_consta
       for (int t = 0; ok && t < nt; ++t) {
         const int sq = t % kNQ, sd = t % kND;
         ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.gdp_full, t & 1, wt));
+        ok = ok && __all_sync(0xffffffffu, mbar_wait(&ctrl.do_full[sd], (t / kND) & 1, wt));
         if (!ok) break;
         tc_fence_after();
         const uint32_t do_mn = desc_lo(sm0 + kDO_OFF + sd * kDO, kQB);
@@ -363,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) bob_cols_wide(const __grid_consta
         mma_commit_w(&ctrl.gdp_empty);
         mma_commit_w(&ctrl.do_empty[sd]);
         ok = __all_sync(0xffffffffu, mbar_wait(&ctrl.kop_full, t & 1, wt));
+        ok = ok && __all_sync(0xffffffffu, mbar_wait(&ctrl.qu_full[sq], (t / kNQ) & 1, wt));
         if (!ok) break;
         tc_fence_after();
         const uint32_t qu_mn = desc_lo(sm0 + kQU_OFF + sq * kQUS, kQUCH);
