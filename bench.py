@@ -54,13 +54,20 @@ SWEEP = ("gpt2s_b8h12_n1024_d64",
          "peaky_b4h32_n8192_d128")
 # Counted GEMMs (2 N^2 d FLOPs each, per head) attributed to each kernel: the
 # 38 N^2 d of BoB = pass 1 (11: S, dP, C, B x2, U1 x2, U2, W, Y x2) + pass 2
-# (8).  Pass 1 runs as two sweeps: U1-and-Y (the five score GEMMs + U1 x2 +
-# Y x2 = 9) and Z (one GEMM doing the work of U2 and W: 2); the recomputed S
-# and dP of the Z sweep are not counted.  Forward 2 (S, PV); first backward
-# 5 (S, dP, dQ in the row kernel, dV, dK in the column kernel; the column
-# kernel's recomputed S and dP are not counted).
-COUNTED_GEMMS = {"bob_pass1_u1y": 9, "bob_pass1_z": 2, "bob_pass2": 8,
+# (8).  At d <= 64 pass 1 is one sweep (bob_pass1: all 11).  At d > 64 it runs
+# as two sweeps: U1-and-Y (the five score GEMMs + U1 x2 + Y x2 = 9) and Z (one
+# GEMM doing the work of U2 and W: 2); the recomputed S and dP of the Z sweep
+# are not counted.  Forward 2 (S, PV; the second P V product of the hi/lo
+# split of P is not counted); first backward 5 (S, dP, dQ in the row kernel,
+# dV, dK in the column kernel; the column kernel's recomputed S and dP are not
+# counted).
+COUNTED_GEMMS = {"bob_pass1": 11, "bob_pass1_u1y": 9, "bob_pass1_z": 2, "bob_pass2": 8,
                  "attn_fwd": 2, "attn_bwd_dq": 3, "attn_bwd_dkdv": 2}
+
+
+def bob_kernels(d):
+    """The launches of one BoB call at head size d."""
+    return ("bob_pass1", "bob_pass2") if d <= 64 else ("bob_pass1_u1y", "bob_pass1_z", "bob_pass2")
 # Resident rows of one CTA: the query-row block of pass 1 (B_r) and the key
 # block of pass 2 (B_c) of every BoB kernel.
 BLOCK_ROWS = 128
@@ -579,6 +586,11 @@ def kernel_bytes(name, N, d, br=BLOCK_ROWS):
     tensors of all N rows.  compulsory: every tensor the kernel touches read
     or written once."""
     Nd, N2 = N * d, N * N / br
+    if name == "bob_pass1":
+        # the one-sweep pass 1: resident Q, UQ, dO, O, L, D; streams K, UK, V, UV;
+        # writes gQ, gdO, (alpha, E)
+        res, stream, out = 6 * Nd + 4 * Nd + 8 * N, 8 * d * N2, 8 * Nd + 8 * N
+        return res + stream + out, res + 8 * Nd + out
     if name == "bob_pass1_u1y":
         # resident Q, UQ, dO (bf16), O, L, D; streams K, UK, V, UV; writes U1 (gQ), gdO, (alpha, E)
         res, stream, out = 6 * Nd + 4 * Nd + 8 * N, 8 * d * N2, 8 * Nd + 8 * N
@@ -599,18 +611,19 @@ def bob_ledger(w, pairs=1.0):
     Strengths, "Theory honestly scoped": Theorem 4.3, Q = 12Nd + 4N +
     4dN^2/B_r + (3d+4)N^2/B_c words per head), in bytes for bf16 inputs and
     fp32 O / vectors / outputs, at B_r = B_c = BLOCK_ROWS, beside the same
-    count for the kernels as built (pass 1 as two sweeps: the Z sweep streams
-    K, V once more and round-trips U1), and measured DRAM bytes per call when
-    the committed counters match the current sources."""
+    count for the kernels as built (at d > 64 pass 1 runs as two sweeps: the
+    Z sweep streams K, V once more and round-trips U1), and measured DRAM
+    bytes per call when the committed counters match the current sources."""
     N, d, h = w.N, w.d, w.B * w.H
     br = bc = BLOCK_ROWS
     pages = h * (34 * N * d + 16 * N + 8 * d * N * N / br + (6 * d + 16) * N * N / bc)
-    built = sum(kernel_bytes(k, N, d)[0] for k in ("bob_pass1_u1y", "bob_pass1_z", "bob_pass2")) * h
-    comp = sum(kernel_bytes(k, N, d)[1] for k in ("bob_pass1_u1y", "bob_pass1_z", "bob_pass2")) * h
+    kern = bob_kernels(d)
+    built = sum(kernel_bytes(k, N, d)[0] for k in kern) * h
+    comp = sum(kernel_bytes(k, N, d)[1] for k in kern) * h
     measured = None
     rec = _traffic_record(w, pairs)
     if rec is not None:
-        got = [rec["kernels"].get(k) for k in ("bob_pass1_u1y", "bob_pass1_z", "bob_pass2")]
+        got = [rec["kernels"].get(k) for k in kern]
         if all(g is not None for g in got):
             measured = sum(g["bytes_per_launch"] * h / g["heads"] for g in got)
     out = {"formula": "Theorem 4.3: 12Nd + 4N + 4dN^2/B_r + (3d+4)N^2/B_c words per head",

@@ -109,12 +109,19 @@ __device__ __forceinline__ void load_tile2(const CUtensorMap* m0, const CUtensor
 // cotangent of S, Sbar = P (Pbar - En) with Pbar = tau B (dP - D) + C - alpha dP
 // and En = sum_j P Pbar, and the kernel writes gQ = tau (dS UK + Sbar K)
 // summed over all keys - no row totals, no correction sweep.
-template <int D_, bool DIRECT = false>
+//
+// FULL (d = 64: the whole of pass 1 in one sweep): TMEM also holds the two
+// remaining alpha-free accumulators U2 += P K and W += dS K (four of 64
+// columns each, one score buffer of 128, Q, UQ, dO 96: 480 of 512), so the
+// row end applies the affine correction gQ = tau (U1 - EX U2 - alpha W)
+// directly and no Z sweep follows.
+template <int D_, bool DIRECT = false, bool FULL = false>
 struct PassU1Y {
   using Params = P1Params;
   static constexpr int D = D_, DC = D / 64, T = 32;
   static constexpr bool kWide = D == 128;
-  static constexpr bool ROWS = true, SPLIT = kWide;
+  static_assert(!FULL || (D == 64 && !DIRECT), "the one-sweep pass 1 fits TMEM at d = 64");
+  static constexpr bool ROWS = true, SPLIT = kWide || FULL;
   static constexpr int TRES = kWide ? 2 : 3;            // Q, UQ (, dO)
   static constexpr int RES = kWide ? DC * kChunk : 0;   // dO in shared memory
   static constexpr int ACH = 4 * kBlk;                  // [K | UK | V | UV] per 64-column chunk
@@ -123,12 +130,12 @@ struct PassU1Y {
   static constexpr bool VEC = false, ROW_SUMS = !DIRECT, TS = false;
   static constexpr int VEC_OFF = 0, NVEC = 0, VEC_SCRATCH = 0;
   static constexpr int OPS = 4 * kChunk;                // dS, X, P, PB tiles; half h = columns 32h..32h+31
-  static constexpr int ACC = 2 * D;                     // U1 | Y
-  static constexpr int SCOLS = 128, NBUF = kWide ? 1 : 2;   // [S|B|dP|C]
+  static constexpr int ACC = (FULL ? 4 : 2) * D;        // U1 | Y (| U2 | W)
+  static constexpr int SCOLS = 128, NBUF = (kWide || FULL) ? 1 : 2;   // [S|B|dP|C]
   static constexpr int OP_HALF = 0, OP_COL = ACC + NBUF * SCOLS;
   static constexpr int TRES_COL = OP_COL;
   static constexpr int SMEM = RES + NSA * SA + OPS;
-  static constexpr int A_U1 = 0, A_Y = D;
+  static constexpr int A_U1 = 0, A_Y = D, A_U2 = 2 * D, A_W = 3 * D;
   static constexpr int NC = SPLIT ? T / 2 : T;          // key columns per warpgroup and tile
   static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
   static_assert(SMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
@@ -172,6 +179,10 @@ struct PassU1Y {
       mma_ss_w(tb + A_U1, op_lo(ops, 1, h, kk), mnmaj(amn, 0, kk), id, 1);           // U1 += X K
       mma_ss_w(tb + A_Y, op_lo(ops, 2, h, kk), mnmaj(amn, 3 * kBlk, kk), id, acc0);  // Y += P UV
       mma_ss_w(tb + A_Y, op_lo(ops, 3, h, kk), mnmaj(amn, 2 * kBlk, kk), id, 1);     // Y += PB V
+      if (FULL) {
+        mma_ss_w(tb + A_U2, op_lo(ops, 2, h, kk), mnmaj(amn, 0, kk), id, acc0);      // U2 += P K
+        mma_ss_w(tb + A_W, op_lo(ops, 0, h, kk), mnmaj(amn, 0, kk), id, acc0);       // W += dS K
+      }
     }
   }
   struct Row {
@@ -256,12 +267,19 @@ struct PassU1Y {
     for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
       float u1[16], y[16], o[16];
       tmem_ld16x2(e.tm + A_U1 + c0, e.tm + A_Y + c0, u1, y);
+      if (FULL) {
+        float u2[16], w2[16];
+        tmem_ld16x2(e.tm + A_U2 + c0, e.tm + A_W + c0, u2, w2);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)   // gQ = tau (U1 - EX U2 - alpha W)
+          u1[j] = p.tau * (u1[j] - fmaf(ex, u2[j], alpha * w2[j]));
+      }
       if (!keep) continue;
       if (DIRECT) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) u1[j] *= p.tau;   // gQ = tau (dS UK + Sbar K)
       }
-      store16(p.gQ + ro + c0, u1);   // two-pass: U1, finished by the Z sweep
+      store16(p.gQ + ro + c0, u1);   // two-pass at d = 128: U1, finished by the Z sweep
       const float4* src = reinterpret_cast<const float4*>(p.O + ro + c0);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -817,9 +835,14 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   P1Params p1;
   if (!make_p1(p1, a, c, false)) return cudaErrorInvalidValue;
   const dim3 grid((a.N + kM - 1) / kM, a.BH);
-  // the Z kernel reads what the U1-and-Y kernel wrote (U1 in gQ, alpha and E)
-  cudaError_t e = launch<PassU1Y<D>>("bob_pass1_u1y", p1, grid, s);
-  if (e == cudaSuccess) e = launch<PassZ<D>>("bob_pass1_z", p1, grid, s);
+  cudaError_t e;
+  if constexpr (D == 64) {
+    e = launch<PassU1Y<64, false, true>>("bob_pass1", p1, grid, s);   // one sweep
+  } else {
+    // the Z kernel reads what the U1-and-Y kernel wrote (U1 in gQ, alpha and E)
+    e = launch<PassU1Y<D>>("bob_pass1_u1y", p1, grid, s);
+    if (e == cudaSuccess) e = launch<PassZ<D>>("bob_pass1_z", p1, grid, s);
+  }
   if (e != cudaSuccess) return e;
   if constexpr (D == 128) return tc_bob_cols_wide(a, c, s);
   else return pass2_d<D>(a, c, grid, s);
