@@ -65,6 +65,15 @@ COUNTED_GEMMS = {"bob_pass1": 11, "bob_pass1_u1y": 9, "bob_pass1_z": 2, "bob_pas
                  "attn_fwd": 2, "attn_bwd_dq": 3, "attn_bwd_dkdv": 2}
 
 
+def executed_gemms(d):
+    """GEMMs of 2 N^2 d the kernels execute per head and BoB call: the 19
+    counted plus recomputed score tiles and split operands.  Two-pass at
+    d <= 64: one-sweep pass 1 (11 + the lo term of P o B) and pass 2 (8); at
+    d > 64: U1-and-Y (9 + 1), Z (3: S, dP recomputed, Z) and pass 2 (8).
+    Four-pass: alpha (S, B: 3), E (5), rows (9), pass 2 (8)."""
+    return {"four_pass": 25, "two_pass": 20 if d <= 64 else 21}
+
+
 def bob_kernels(d):
     """The launches of one BoB call at head size d."""
     return ("bob_pass1", "bob_pass2") if d <= 64 else ("bob_pass1_u1y", "bob_pass1_z", "bob_pass2")
@@ -372,12 +381,12 @@ def run_ours(args, w):
                     "peak_kind": f"{pk_kind} burst (bf16_tflops)", "counted_flops": flops_bob},
             "step": {"ms": round(step_ms, 4), "tflops": round(job_tflops(ws, flops_step, step_ms), 3)},
             # the two-pass schedule against the four-pass one it collapses (same counted
-            # 38 N^2 d; the four-pass schedule executes 25 GEMMs per head, two-pass 20)
+            # 38 N^2 d; executed GEMMs per head in the json)
             "ablation_four_pass": {"ms_per_call": round(four_ms, 4),
                                    "tflops_counted": round(flops_bob / (four_ms * 1e-3) / 1e12, 3),
                                    "two_pass_ms_per_call": round(bob_ms, 4),
                                    "two_pass_speedup": round(four_ms / bob_ms, 3),
-                                   "gemms_executed_per_head": {"four_pass": 25, "two_pass": 20}},
+                                   "gemms_executed_per_head": executed_gemms(w.d)},
             "e2e": e2e,
             # our kernels launched in the timed region: K steps x the launches per
             # step the library recorded in the profiling repeat
@@ -420,11 +429,20 @@ def run_sweep(args, fb, torch, dev, stream, peak, headline):
         n = max(5, min(200, int(250.0 / max(one, 1e-3))))
         ms = time_calls(torch, stream, ch.bob, n, warmup=0)
         fb.device_status()
+        # per-kernel times: a separate repeat with the library's per-launch events
+        fb.fbob_profile_report()
+        fb.fbob_profile_enable(True)
+        for _ in range(3):
+            ch.bob()
+        torch.cuda.synchronize()
+        fb.fbob_profile_enable(False)
+        kern = {k: round(v[1] / v[0], 4) for k, v in fb.fbob_profile_report().items()}
         pairs = causal_fraction(w.N) if args.causal else 1.0
         flops = FLOPS_BOB * w.N * w.N * w.d * w.B * w.H * pairs
         tf = flops / (ms * 1e-3) / 1e12
         out.append({"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "calls": n,
                     "ms_per_call": round(ms, 4), "tflops": round(tf, 3), "frac_of_peak": round(tf / peak, 4),
+                    "kernel_avg_ms": kern,
                     "peak_allocated_bytes": int(torch.cuda.max_memory_allocated() - base),
                     "one_nxn_fp32_bytes": 4 * w.N * w.N * w.B * w.H})
         del ch

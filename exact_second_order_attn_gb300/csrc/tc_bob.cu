@@ -110,6 +110,13 @@ __device__ __forceinline__ void load_tile2(const CUtensorMap* m0, const CUtensor
 // and En = sum_j P Pbar, and the kernel writes gQ = tau (dS UK + Sbar K)
 // summed over all keys - no row totals, no correction sweep.
 //
+// The fourth operand P o B enters gdO = Y - alpha O, which on a peaked
+// softmax row nearly cancels (P o B ~ alpha P on the dominant key); one bf16
+// rounding of it would show in gdO at a few 1e-3 of its maximum.  So the
+// two-pass sweeps carry it as two bf16 terms, PB = PB_hi + PB_lo (a fifth
+// operand tile and one more MMA per 16 keys).  DIRECT knows alpha and instead
+// writes the centred P o (B - alpha) (gdO = Y, nothing cancels).
+//
 // FULL (d = 64: the whole of pass 1 in one sweep): TMEM also holds the two
 // remaining alpha-free accumulators U2 += P K and W += dS K (four of 64
 // columns each, one score buffer of 128, Q, UQ, dO 96: 480 of 512), so the
@@ -126,10 +133,12 @@ struct PassU1Y {
   static constexpr int RES = kWide ? DC * kChunk : 0;   // dO in shared memory
   static constexpr int ACH = 4 * kBlk;                  // [K | UK | V | UV] per 64-column chunk
   static constexpr int SA = DC * ACH, SA_TX = SA, SB = 0, SB_TX = 0;
-  static constexpr int NSA = kWide ? 4 : 8, NSB = 0;
+  static constexpr bool kSplitPB = !DIRECT;             // PB as bf16 hi + lo (see above)
+  static constexpr int NSA = kWide ? (kSplitPB ? 3 : 4) : 8, NSB = 0;
   static constexpr bool VEC = false, ROW_SUMS = !DIRECT, TS = false;
   static constexpr int VEC_OFF = 0, NVEC = 0, VEC_SCRATCH = 0;
-  static constexpr int OPS = 4 * kChunk;                // dS, X, P, PB tiles; half h = columns 32h..32h+31
+  // dS, X, P, PB (, PB_lo) tiles; half h = columns 32h..32h+31
+  static constexpr int OPS = (kSplitPB ? 5 : 4) * kChunk;
   static constexpr int ACC = (FULL ? 4 : 2) * D;        // U1 | Y (| U2 | W)
   static constexpr int SCOLS = 128, NBUF = (kWide || FULL) ? 1 : 2;   // [S|B|dP|C]
   static constexpr int OP_HALF = 0, OP_COL = ACC + NBUF * SCOLS;
@@ -179,6 +188,7 @@ struct PassU1Y {
       mma_ss_w(tb + A_U1, op_lo(ops, 1, h, kk), mnmaj(amn, 0, kk), id, 1);           // U1 += X K
       mma_ss_w(tb + A_Y, op_lo(ops, 2, h, kk), mnmaj(amn, 3 * kBlk, kk), id, acc0);  // Y += P UV
       mma_ss_w(tb + A_Y, op_lo(ops, 3, h, kk), mnmaj(amn, 2 * kBlk, kk), id, 1);     // Y += PB V
+      if (kSplitPB) mma_ss_w(tb + A_Y, op_lo(ops, 4, h, kk), mnmaj(amn, 2 * kBlk, kk), id, 1);  // + PB_lo V
       if (FULL) {
         mma_ss_w(tb + A_U2, op_lo(ops, 2, h, kk), mnmaj(amn, 0, kk), id, acc0);      // U2 += P K
         mma_ss_w(tb + A_W, op_lo(ops, 0, h, kk), mnmaj(amn, 0, kk), id, acc0);       // W += dS K
@@ -218,7 +228,7 @@ struct PassU1Y {
       const uint32_t c = a.sc + a.c0 + q * 16;
       tmem_ld16x4(c, c + 32, c + 64, c + 96, S, B, dP, C);
       if (q == NC / 16 - 1) s.release_scores();
-      uint32_t wdS[8], wX[8], wP[8], wPB[8];
+      uint32_t wdS[8], wX[8], wP[8], wPB[8], wPBl[8];
 #pragma unroll
       for (int j = 0; j < 16; j += 2) {
         float ds[2], x[2], pv[2], pb[2];
@@ -229,12 +239,13 @@ struct PassU1Y {
           const float be = p.tau * B[j + e];
           const float te = dP[j + e] - w.Di;
           pv[e] = pe;
-          pb[e] = pe * be;
           ds[e] = pe * te;
           if (DIRECT) {
+            pb[e] = pe * (be - w.alpha);   // the centred P o (B - alpha)
             // Sbar = P (tau B (dP - D) + C - alpha dP - En)
             x[e] = pe * (fmaf(be, te, C[j + e]) - fmaf(w.alpha, dP[j + e], w.ex));
           } else {
+            pb[e] = pe * be;
             w.alpha += pb[e];
             x[e] = pe * fmaf(be, te, C[j + e]);
             w.ex += x[e];
@@ -243,7 +254,12 @@ struct PassU1Y {
         wdS[j / 2] = pack_bf16x2(ds[0], ds[1]);
         wX[j / 2] = pack_bf16x2(x[0], x[1]);
         wP[j / 2] = pack_bf16x2(pv[0], pv[1]);
-        wPB[j / 2] = pack_bf16x2(pb[0], pb[1]);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(pb[0], pb[1]);
+        wPB[j / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+        if (kSplitPB) {
+          const float2 hf = __bfloat1622float2(hi);
+          wPBl[j / 2] = pack_bf16x2(pb[0] - hf.x, pb[1] - hf.y);   // exact differences, rounded once more
+        }
       }
       if (!kEarly && !s.acquire_ops()) return false;
       const int col = 32 * (int)a.h + a.c0 + q * 16;
@@ -251,6 +267,7 @@ struct PassU1Y {
       write_op_cols<8>(a.ops + kChunk, (uint32_t)r, col, wX);
       write_op_cols<8>(a.ops + 2 * kChunk, (uint32_t)r, col, wP);
       write_op_cols<8>(a.ops + 3 * kChunk, (uint32_t)r, col, wPB);
+      if (kSplitPB) write_op_cols<8>(a.ops + 4 * kChunk, (uint32_t)r, col, wPBl);
     }
     s.publish_ops();
     return true;
@@ -280,6 +297,10 @@ struct PassU1Y {
         for (int j = 0; j < 16; ++j) u1[j] *= p.tau;   // gQ = tau (dS UK + Sbar K)
       }
       store16(p.gQ + ro + c0, u1);   // two-pass at d = 128: U1, finished by the Z sweep
+      if (DIRECT) {
+        store16(p.gdO + ro + c0, y);   // gdO = P UV + P o (B - alpha) V
+        continue;
+      }
       const float4* src = reinterpret_cast<const float4*>(p.O + ro + c0);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {

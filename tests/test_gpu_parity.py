@@ -30,6 +30,10 @@ BF16_TOL = 1e-2
 FP32_TOL = 2e-5
 CLOSED_FORM_TOL = 1e-5
 KEYS = ("O", "L", "dQ", "dK", "dV", "D", "gQ", "gK", "gV", "gdO", "alpha", "E")
+# Peaked softmax rows (Q, K with std 4) are where bf16 operand roundings meet
+# cancellations (dP - D and Y - alpha O on a row's dominant key); those seeds
+# are held to 0.7 of the bf16 bar so that the margin is visible.
+PEAKY_MARGIN_TOL = 0.7 * BF16_TOL
 # Identity residuals at any size: <gdO, dO> - f and <gV, V> - (<UQ,dQ> + <UK,dK>)
 # are random-sign sums of per-element errors, and so are the reference sums,
 # so their ratio is of the order of the per-element relative error: bf16
@@ -164,7 +168,8 @@ def test_d128_workloads_sampled_heads(name, heads, seed):
     w = dataclasses.replace(attn_inputs.WORKLOADS[name], seed=seed)
     gpu, inp = run_chain(w)
     ref = oracle_chain(oracle_inputs(inp, heads), w.tau)
-    compare_all(select_heads(gpu, heads), ref, BF16_TOL, case=f"{name}:seed{seed}")
+    tol = PEAKY_MARGIN_TOL if name.startswith("peaky") else BF16_TOL
+    compare_all(select_heads(gpu, heads), ref, tol, case=f"{name}:seed{seed}")
     # every head: finite, and the exact key-side properties
     for k, v in gpu.items():
         assert np.isfinite(v).all(), k
