@@ -73,6 +73,8 @@ __all__ = [
     "bob_row_scalars",
     "bob_four_pass_rows",
     "attn_bob_four_pass",
+    "bob_sampled_rows",
+    "bob_sampled_cols",
 ]
 
 # Largest number of fp64 score elements one row block materialises
@@ -415,3 +417,64 @@ def bob_sampled_rows(Q, K, V, dO, UQ, UK, UV, tau, rows, causal=False):
     gQ, _, _, gdO = bob_rows(_f64(Q)[rows], K, V, _f64(dO)[rows], _f64(UQ)[rows], UK, UV, tau,
                              rows if causal else None)
     return gQ, gdO
+
+
+def _bob_cols_block(Q, K, V, dO, UQ, UK, UV, tau, cols, rows, causal):
+    """One query-row block's contribution to the key-side outputs at the key
+    rows ``cols`` (see ``bob_sampled_cols``)."""
+    qidx = _qidx(rows, causal)
+    Qr, dOr, UQr = Q[rows], dO[rows], UQ[rows]
+    # forward sweep over every key: the row reductions need whole rows
+    S = _mask(tau * (Qr @ K.T), qidx)
+    P, _ = _softmax_rows(S)
+    O = P @ V
+    dP = dOr @ V.T
+    D = (dOr * O).sum(axis=1)
+    # reverse sweep of bob_rows up to its two row reductions
+    dS_bar = tau * (UQr @ K.T + Qr @ UK.T)         # from the dQ and dK seeds
+    D_bar = -(dS_bar * P).sum(axis=1)
+    O_bar = D_bar[:, None] * dOr
+    # P_bar = dO UV^T + dS_bar o (dP - D) + O_bar V^T, with O_bar V^T = D_bar dP
+    P_bar = dOr @ UV.T + dS_bar * (dP - D[:, None]) + D_bar[:, None] * dP
+    centre = (P * P_bar).sum(axis=1)
+    # the rest of the sweep acts entry by entry: keep only the sampled keys
+    Pj, dPj, dS_barj, P_barj = P[:, cols], dP[:, cols], dS_bar[:, cols], P_bar[:, cols]
+    dSj = Pj * (dPj - D[:, None])
+    S_barj = Pj * (P_barj - centre[:, None])
+    dP_barj = dS_barj * Pj
+    dK = tau * (dSj.T @ Qr)
+    dV = Pj.T @ dOr
+    gK = tau * (dSj.T @ UQr) + tau * (S_barj.T @ Qr)
+    gV = dP_barj.T @ dOr + Pj.T @ O_bar
+    return dK, dV, gK, gV
+
+
+def bob_sampled_cols(Q, K, V, dO, UQ, UK, UV, tau, cols, causal=False, workers=1):
+    """Key-side outputs (dK, dV, gK, gV) of one head restricted to the key rows
+    ``cols``.
+
+    A key row's outputs are sums over all query rows, and each query row's
+    term needs three reductions over all of that row's keys: the softmax
+    normaliser, D, and in the reverse sweep of ``bob_rows`` the adjoint of D
+    (minus alpha) and the centre rowsum(P o P_bar) of the softmax reverse step.
+    So every query-row block is swept over all keys up to those reductions; the
+    remaining steps act on single entries and are taken on the sampled key
+    columns only before the contraction over the block's query rows.
+    ``workers`` > 1 runs the independent row blocks on that many threads; the
+    partial sums are added in block order either way.
+    """
+    cols = np.asarray(cols)
+    args = tuple(_f64(a) for a in (Q, K, V, dO, UQ, UK, UV))
+    blocks = list(_row_blocks(args[0].shape[0]))
+    run = lambda rows: _bob_cols_block(*args, tau, cols, rows, causal)
+    if workers > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(workers) as ex:
+            parts = list(ex.map(run, blocks))
+    else:
+        parts = [run(rows) for rows in blocks]
+    out = [np.zeros((len(cols), a.shape[1])) for a in (args[1], args[2], args[1], args[2])]
+    for part in parts:
+        for o, p in zip(out, part):
+            o += p
+    return tuple(out)

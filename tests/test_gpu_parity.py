@@ -158,6 +158,23 @@ def test_long_context_sampled_rows(N):
     sampled_row_checks(w, gpu, inp, rows)
 
 
+def test_long_context_sampled_key_rows():
+    """Key-side outputs (dK, dV, gK, gV) at N = 65536 element by element on
+    sampled key rows: tile edges, the middle and the last rows.  A key row's
+    outputs sum over every query row, so the oracle sweeps all query rows up
+    to their row reductions and keeps only the sampled keys after that."""
+    N = 65536
+    w = attn_inputs.WORKLOADS[f"long_context_b1h1_d64@N={N}"]
+    gpu, inp = run_chain(w)
+    x = {k: v[0, 0].double().numpy() for k, v in inp.items()}
+    cols = [0, 1, 127, 128, N // 2 + 3, N - 129, N - 1]
+    args = [x[k] for k in ("Q", "K", "V", "dO", "UQ", "UK", "UV")]
+    ref = orc.bob_sampled_cols(*args, w.tau, cols, workers=os.cpu_count() or 1)
+    errs = {k: rel_err(gpu[k][0, 0][cols], r) for k, r in zip(("dK", "dV", "gK", "gV"), ref)}
+    log_errors("long_context_sampled_key_rows", errs)
+    assert all(e <= BF16_TOL for e in errs.values()), errs
+
+
 @pytest.mark.parametrize("name,heads,seed", [
     ("wide_head_b2h16_n16384_d128", [(0, 0), (1, 15)], 0),
     ("peaky_b4h32_n8192_d128", [(0, 0), (3, 31)], 0),

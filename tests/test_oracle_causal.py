@@ -106,6 +106,11 @@ def test_causal_row_blocking_and_sampling(monkeypatch):
     sq, so = orc.bob_sampled_rows(*(x[1] for x in X), tau, rows, causal=True)
     np.testing.assert_allclose(sq, full[0][1][rows], rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(so, full[3][1][rows], rtol=1e-12, atol=1e-13)
+    _, dK, dV, _ = orc.attn_bwd(*X[:4], tau, causal=True)
+    cols = [0, 7, 48, 49]
+    got = orc.bob_sampled_cols(*(x[1] for x in X), tau, cols, causal=True)
+    for g, ref in zip(got, (dK[1], dV[1], full[1][1], full[2][1])):
+        np.testing.assert_allclose(g, ref[cols], rtol=1e-12, atol=1e-13)
     monkeypatch.setattr(orc, "_BLOCK_ELEMS", 4 * N)      # 4-row blocks, ragged tail
     blocked = orc.attn_bob(*X, tau, causal=True)
     for a, b in zip(full, blocked):

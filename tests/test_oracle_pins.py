@@ -314,3 +314,20 @@ def test_sampled_rows_match_full():
     sq, so = orc.bob_sampled_rows(*X, tau, rows)
     np.testing.assert_allclose(sq, gQ[rows], rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(so, gdO[rows], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("block_rows,workers", [(None, 1), (5, 3)])
+def test_sampled_key_rows_match_full(monkeypatch, block_rows, workers):
+    """The key-side sample (every query row swept, sampled key columns kept)
+    equals the full sweep's key rows, for whole and for ragged row blocks."""
+    rng = np.random.default_rng(16)
+    N, d, tau = 64, 8, 0.5
+    X = [x[0] for x in inputs(rng, N, d)]
+    _, gK, gV, _ = orc.attn_bob(*X, tau)
+    _, dK, dV, _ = orc.attn_bwd(*X[:4], tau)
+    if block_rows:
+        monkeypatch.setattr(orc, "_BLOCK_ELEMS", block_rows * N)
+    cols = [0, 1, 31, 62, 63]
+    got = orc.bob_sampled_cols(*X, tau, cols, workers=workers)
+    for g, ref in zip(got, (dK, dV, gK, gV)):
+        np.testing.assert_allclose(g, ref[cols], rtol=1e-12, atol=1e-13)
