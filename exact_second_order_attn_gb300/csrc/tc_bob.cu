@@ -144,7 +144,13 @@ struct PassU1Y {
   static constexpr int OP_HALF = 0, OP_COL = ACC + NBUF * SCOLS;
   static constexpr int TRES_COL = OP_COL;
   static constexpr int SMEM = RES + NSA * SA + OPS;
-  static constexpr int A_U1 = 0, A_Y = D, A_U2 = 2 * D, A_W = 3 * D;
+  // Ring-A order of the four 32-row blocks: [K | UK | V | UV], or with FULL
+  // [V | UV | K | UK], where UV, K and K, UK are neighbours, so that two
+  // pairs of accumulator products share their A operand as one N = 2d MMA:
+  // P [UV | K] -> [Y | U2] and dS [K | UK] -> [W | U1] (TMEM Y | U2 | W | U1).
+  static constexpr int BK = FULL ? 2 : 0, BUK = BK + 1, BV = FULL ? 0 : 2, BUV = BV + 1;
+  static constexpr int A_U1 = FULL ? 3 * D : 0, A_Y = FULL ? 0 : D, A_U2 = FULL ? D : 2 * D, A_W = FULL ? 2 * D : 3 * D;
+  static_assert(!FULL || (A_U2 == A_Y + D && A_U1 == A_W + D), "paired accumulators are adjacent");
   static constexpr int NC = SPLIT ? T / 2 : T;          // key columns per warpgroup and tile
   static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
   static_assert(SMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
@@ -156,8 +162,8 @@ struct PassU1Y {
     for (int kc = 0; kc < DC; ++kc) tma_load_3d(res + kc * kChunk, &p.mdO_res, bar, kc * 64, row0, head);
   }
   __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head, bool) {
-    load_tile2(&p.mK, &p.mUK, st, DC, ACH, kBlk, bar, t * T, head);
-    load_tile2(&p.mV, &p.mUV, st + 2 * kBlk, DC, ACH, kBlk, bar, t * T, head);
+    load_tile2(&p.mK, &p.mUK, st + BK * kBlk, DC, ACH, kBlk, bar, t * T, head);
+    load_tile2(&p.mV, &p.mUV, st + BV * kBlk, DC, ACH, kBlk, bar, t * T, head);
   }
   __device__ static void load_b(const Params&, uint8_t*, uint64_t*, int, int) {}
   __device__ static void fill_vec(const Params&, float*, int, int, int) {}
@@ -166,16 +172,16 @@ struct PassU1Y {
     const uint32_t i64 = idesc_bf16(kM, 64, false, false), i32 = idesc_bf16(kM, 32, false, false);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k)  // [S | Q UK^T] = Q [K; UK]^T
-      mma_ts_w(sc, tres_a(tres, 0, D, k), kmaj(sa, ACH, 0, k), i64, k > 0);
+      mma_ts_w(sc, tres_a(tres, 0, D, k), kmaj(sa, ACH, BK * kBlk, k), i64, k > 0);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k)  // B += UQ K^T
-      mma_ts_w(sc + 32, tres_a(tres, 1, D, k), kmaj(sa, ACH, 0, k), i32, 1);
+      mma_ts_w(sc + 32, tres_a(tres, 1, D, k), kmaj(sa, ACH, BK * kBlk, k), i32, 1);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {  // [dP | C] = dO [V; UV]^T
       if (kWide)
-        mma_ss_w(sc + 64, res_lo(res, 0, DC, k), kmaj(sa, ACH, 2 * kBlk, k), i64, k > 0);
+        mma_ss_w(sc + 64, res_lo(res, 0, DC, k), kmaj(sa, ACH, BV * kBlk, k), i64, k > 0);
       else
-        mma_ts_w(sc + 64, tres_a(tres, 2, D, k), kmaj(sa, ACH, 2 * kBlk, k), i64, k > 0);
+        mma_ts_w(sc + 64, tres_a(tres, 2, D, k), kmaj(sa, ACH, BV * kBlk, k), i64, k > 0);
     }
   }
   __device__ static void accum_mmas(uint32_t tb, uint32_t ops, uint32_t sa, uint32_t h, bool first) {
@@ -184,14 +190,21 @@ struct PassU1Y {
 #pragma unroll
     for (int kk = 0; kk < T / 16; ++kk) {
       const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
-      mma_ss_w(tb + A_U1, op_lo(ops, 0, h, kk), mnmaj(amn, kBlk, kk), id, acc0);     // U1 += dS UK
-      mma_ss_w(tb + A_U1, op_lo(ops, 1, h, kk), mnmaj(amn, 0, kk), id, 1);           // U1 += X K
-      mma_ss_w(tb + A_Y, op_lo(ops, 2, h, kk), mnmaj(amn, 3 * kBlk, kk), id, acc0);  // Y += P UV
-      mma_ss_w(tb + A_Y, op_lo(ops, 3, h, kk), mnmaj(amn, 2 * kBlk, kk), id, 1);     // Y += PB V
-      if (kSplitPB) mma_ss_w(tb + A_Y, op_lo(ops, 4, h, kk), mnmaj(amn, 2 * kBlk, kk), id, 1);  // + PB_lo V
-      if (FULL) {
-        mma_ss_w(tb + A_U2, op_lo(ops, 2, h, kk), mnmaj(amn, 0, kk), id, acc0);      // U2 += P K
-        mma_ss_w(tb + A_W, op_lo(ops, 0, h, kk), mnmaj(amn, 0, kk), id, acc0);       // W += dS K
+      if constexpr (FULL) {
+        // N = 2d over two neighbouring 64-column blocks: LBO = one block
+        const uint32_t amn2 = desc_lo(sa, kBlk);
+        const uint32_t id2 = idesc_bf16(kM, 2 * D, false, true);
+        mma_ss_w(tb + A_Y, op_lo(ops, 2, h, kk), mnmaj(amn2, BUV * kBlk, kk), id2, acc0);  // [Y | U2] += P [UV | K]
+        mma_ss_w(tb + A_Y, op_lo(ops, 3, h, kk), mnmaj(amn, BV * kBlk, kk), id, 1);        // Y += PB V
+        mma_ss_w(tb + A_Y, op_lo(ops, 4, h, kk), mnmaj(amn, BV * kBlk, kk), id, 1);        // + PB_lo V
+        mma_ss_w(tb + A_W, op_lo(ops, 0, h, kk), mnmaj(amn2, BK * kBlk, kk), id2, acc0);   // [W | U1] += dS [K | UK]
+        mma_ss_w(tb + A_U1, op_lo(ops, 1, h, kk), mnmaj(amn, BK * kBlk, kk), id, 1);       // U1 += X K
+      } else {
+        mma_ss_w(tb + A_U1, op_lo(ops, 0, h, kk), mnmaj(amn, BUK * kBlk, kk), id, acc0);   // U1 += dS UK
+        mma_ss_w(tb + A_U1, op_lo(ops, 1, h, kk), mnmaj(amn, BK * kBlk, kk), id, 1);       // U1 += X K
+        mma_ss_w(tb + A_Y, op_lo(ops, 2, h, kk), mnmaj(amn, BUV * kBlk, kk), id, acc0);    // Y += P UV
+        mma_ss_w(tb + A_Y, op_lo(ops, 3, h, kk), mnmaj(amn, BV * kBlk, kk), id, 1);        // Y += PB V
+        if (kSplitPB) mma_ss_w(tb + A_Y, op_lo(ops, 4, h, kk), mnmaj(amn, BV * kBlk, kk), id, 1);  // + PB_lo V
       }
     }
   }
@@ -615,7 +628,8 @@ struct Pass2 {
   static constexpr int TRES_COL = OP_COL + (kAllTmem ? 2 * OP_HALF : 0);
   static constexpr int NVEC = 4;                   // L, D, (alpha, E) per query
   static constexpr int VEC_SCRATCH = RES + NSA * SA + OPS;   // 2 warpgroups x 2 buffers x NVEC x T floats
-  static constexpr int SMEM = VEC_SCRATCH + 4 * NVEC * T * 4;
+  static constexpr int QREC = VEC_SCRATCH + 4 * NVEC * T * 4; // per elementwise warp: T query records
+  static constexpr int SMEM = QREC + kEwWarps * T * 16;
   static_assert(TRES_COL + TRES * D / 2 <= 512, "TMEM budget");
   static_assert(SMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
   static constexpr int A_K = 0, A_V = D;
@@ -706,10 +720,20 @@ struct Pass2 {
   static constexpr int NC = SPLIT ? T / 2 : T;
   template <bool MASK>
   __device__ static bool ew_tile(Row&, const Params& p, const TileArgs& a, const TileSync& s, int r) {
+    static_assert(NC == 32, "one query record per lane");
     const float sc = p.tau * kLog2e;
-    const float* vL = a.vec + a.c0;
-    const float* vD = a.vec + T + a.c0;
-    const float2* vAE = reinterpret_cast<const float2*>(a.vec + 2 * T) + a.c0;
+    // The tile's per-query constants, formed once per warp instead of once
+    // per (key, query): (-L log2e, D, alpha, alpha D - E) in this warp's own
+    // records (no other warp reads them, so a warp barrier orders them).
+    float4* rec = reinterpret_cast<float4*>(a.smem + QREC) + (threadIdx.x >> 5) * T;
+    {
+      const int i = a.c0 + (int)(threadIdx.x & 31u);
+      const float Lq = a.vec[i], Dq = a.vec[T + i];
+      const float2 ae = reinterpret_cast<const float2*>(a.vec + 2 * T)[i];
+      __syncwarp();   // every lane has read the previous tile's records
+      rec[threadIdx.x & 31u] = make_float4(-Lq * kLog2e, Dq, ae.x, fmaf(ae.x, Dq, -ae.y));
+      __syncwarp();
+    }
     // one score buffer: its release comes first, the operands are taken after
     uint32_t wdS[NC / 2], wGs[NC / 2], wGd[NC / 2];
 #pragma unroll
@@ -724,14 +748,13 @@ struct Pass2 {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int ii = q * 16 + j + e;   // query column (relative to a.c0)
-          const float Dq = vD[ii];
-          const float2 ae = vAE[ii];
+          const float4 v = rec[ii];
           const int col = a.c0 + ii;         // tile column (query)
-          const float pe = (!MASK || (col >= a.lo && col <= a.hi)) ? ex2(fmaf(S[j + e], sc, -vL[ii] * kLog2e)) : 0.f;
-          const float te = dP[j + e] - Dq;
-          const float bp = fmaf(p.tau, B[j + e], -ae.x);
+          const float pe = (!MASK || (col >= a.lo && col <= a.hi)) ? ex2(fmaf(S[j + e], sc, v.x)) : 0.f;
+          const float te = dP[j + e] - v.y;
+          const float bp = fmaf(p.tau, B[j + e], -v.z);
           dsv[e] = pe * te;
-          gsv[e] = pe * (fmaf(bp, te, C[j + e]) + fmaf(ae.x, Dq, -ae.y));
+          gsv[e] = pe * (fmaf(bp, te, C[j + e]) + v.w);
           gdv[e] = pe * bp;
         }
         const int k = q * 8 + j / 2;

@@ -67,7 +67,8 @@ constexpr int kRES_OFF = 0;                // K (2 chunks), UK (2 chunks)
 constexpr int kQU_OFF = kRES_OFF + 2 * kDC * kChunk;
 constexpr int kDO_OFF = kQU_OFF + kNQ * kQUS;
 constexpr int kOPS_OFF = kDO_OFF + kND * kDO;   // Gdp, dS, Gs tiles [128][64]
-constexpr int kSMEM = kOPS_OFF + 3 * kChunk;
+constexpr int kREC_OFF = kOPS_OFF + 3 * kChunk; // per elementwise warp: 2 x 32 float2 query records
+constexpr int kSMEM = kREC_OFF + 8 * 64 * 8;
 static_assert(kQUS % 1024 == 0 && kQU_OFF % 1024 == 0 && kDO_OFF % 1024 == 0 && kOPS_OFF % 1024 == 0,
               "1024-byte aligned tiles");
 static_assert(kSMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
@@ -122,11 +123,23 @@ __device__ __forceinline__ void fill_vectors(const ColParams& p, float* vec, int
 // queries past N) and gets P = 0.  Returns false when a wait gave up.
 template <bool MASK>
 __device__ __forceinline__ bool ew_tile(const ColParams& p, ColCtrl& c, const Waiter& wt, uint32_t sc_col,
-                                        uint32_t ops, const float* vec, int t, int c0, int lo, int hi, int r) {
+                                        uint32_t ops, const float* vec, float2* rec, int t, int c0, int lo, int hi,
+                                        int r) {
   const float sc = p.tau * kLog2e;
-  const float* vL = vec + c0;
-  const float* vD = vec + kQT + c0;
-  const float2* vAE = reinterpret_cast<const float2*>(vec + 2 * kQT) + c0;
+  // The tile's per-query constants, formed once per warp instead of once per
+  // (key, query): (-L log2e, alpha) for phase A and (D, alpha D - E) for
+  // phase B, in this warp's own records (a warp barrier orders them).
+  float2* recA = rec;
+  float2* recB = rec + 32;
+  {
+    const int lane = (int)(threadIdx.x & 31u), i = c0 + lane;
+    const float Lq = vec[i], Dq = vec[kQT + i];
+    const float2 ae = reinterpret_cast<const float2*>(vec + 2 * kQT)[i];
+    __syncwarp();   // every lane has read the previous tile's records
+    recA[lane] = make_float2(-Lq * kLog2e, ae.x);
+    recB[lane] = make_float2(Dq, fmaf(ae.x, Dq, -ae.y));
+    __syncwarp();
+  }
   float P[32], bp[32];
   // ---- phase A: S^T and B^T / tau of this warpgroup's 32 queries
   if (!__all_sync(0xffffffffu, mbar_wait(&c.s_full[0], t & 1, wt))) return false;
@@ -139,8 +152,9 @@ __device__ __forceinline__ bool ew_tile(const ColParams& p, ColCtrl& c, const Wa
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int col = c0 + j;
-      P[j] = (!MASK || (col >= lo && col <= hi)) ? ex2(fmaf(S[j], sc, -vL[j] * kLog2e)) : 0.f;
-      bp[j] = fmaf(p.tau, B[j], -vAE[j].x);
+      const float2 v = recA[j];
+      P[j] = (!MASK || (col >= lo && col <= hi)) ? ex2(fmaf(S[j], sc, v.x)) : 0.f;
+      bp[j] = fmaf(p.tau, B[j], -v.y);
     }
   }
   // Gdp = P b' for gV; the previous tile's gV MMAs must have read the tile
@@ -170,11 +184,10 @@ __device__ __forceinline__ bool ew_tile(const ColParams& p, ColCtrl& c, const Wa
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int k = 16 * h + j + e;
-        const float Dq = vD[k];
-        const float2 ae = vAE[k];
-        const float te = dP[k] - Dq;
+        const float2 v = recB[k];
+        const float te = dP[k] - v.x;
         ds[e] = P[k] * te;
-        gs[e] = P[k] * (fmaf(bp[k], te, C[k]) + fmaf(ae.x, Dq, -ae.y));
+        gs[e] = P[k] * (fmaf(bp[k], te, C[k]) + v.y);
       }
       wd[j / 2] = pack_bf16x2(ds[0], ds[1]);
       wg[j / 2] = pack_bf16x2(gs[0], gs[1]);
@@ -415,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) bob_cols_wide(const __grid_consta
     const int c0 = 32 * g;
     const uint32_t sc_col = tb + lane + kSC + (uint32_t)c0;
     const uint32_t ops = sm0 + kOPS_OFF;
+    float2* rec = reinterpret_cast<float2*>(smem + kREC_OFF) + warp * 64;
     bool ok = live;
     for (int t = 0; t < nt && ok; ++t) {
       const int tq = t_begin + t;
@@ -429,9 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1) bob_cols_wide(const __grid_consta
       // keeps the choice warp-uniform
       constexpr bool kMask = CAUSAL || RAGGED;
       if (kMask && __any_sync(0xffffffffu, lo > c0 || hi < c0 + 31))
-        ok = ew_tile<kMask>(p, ctrl, wt, sc_col, ops, vec, t, c0, lo, hi, r);
+        ok = ew_tile<kMask>(p, ctrl, wt, sc_col, ops, vec, rec, t, c0, lo, hi, r);
       else
-        ok = ew_tile<false>(p, ctrl, wt, sc_col, ops, vec, t, c0, lo, hi, r);
+        ok = ew_tile<false>(p, ctrl, wt, sc_col, ops, vec, rec, t, c0, lo, hi, r);
     }
     if (ok && __all_sync(0xffffffffu, mbar_wait(&ctrl.acc_full, 0, wt))) {
       tc_fence_after();

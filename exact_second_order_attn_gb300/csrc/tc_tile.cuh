@@ -188,6 +188,7 @@ struct TileArgs {
   int t;               // streamed tile index (data)
   int c0;              // first tile column this warpgroup handles (0, or T/2 when the columns are split)
   int lo, hi;          // tile columns [lo, hi] this thread's row may see (causal mask; else [0, T-1])
+  uint8_t* smem;       // the kernel's dynamic shared memory (policy scratch at the policy's offsets)
 };
 
 // CAUSAL and RAGGED (N not a multiple of 128) are compile-time choices, so
@@ -453,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
       ta.h = (uint32_t)q;
       ta.t = t_begin + t;
       ta.c0 = kSplit ? g * (Op::T / 2) : 0;
+      ta.smem = smem;
       // causal: column c of the tile is key / query (t_begin + t) T + c
       const int diag = blk0 + r - ta.t * Op::T;   // this row's own index, as a tile column
       ta.lo = (CAUSAL && !Op::ROWS) ? diag : 0;
