@@ -30,9 +30,14 @@
 // phase A is read.  The tensor pipe thus sees
 //   A(t)  gK(t-1)  B(t)  gV(t)  A(t+1)  gK(t)  ...
 // with each score phase's read-out covered by an accumulator batch.  dO
-// streams through a ring of its own (released once gV(t) and B(t) are done);
-// [Q | UQ] and the per-query vectors (L, D, alpha, E) through another
-// (released by gK(t)).
+// streams through a one-stage ring of its own (released once gV(t) and B(t)
+// are done: the next dO is needed only by B(t+1), behind A(t+1) and
+// gK(t)); [Q | UQ] and the per-query vectors (L, D, alpha, E) through a
+// three-stage ring released by gK(t).  gK(t) runs after A(t+1), so with two
+// stages the load for tile t+2 could start only once gK(t) had finished and
+// A(t+2) waited for it; the third stage is paid for by the single dO stage
+// and by Gdp and dS sharing one operand tile (Gdp(t) is written once gK(t-1)
+// has read dS(t-1), dS(t) once gV(t) has read Gdp(t)).
 //
 // CTA of 11 warps: warps 0-7 two elementwise warpgroups (both on every tile,
 // warpgroup g on query columns 32g..32g+31; thread r owns TMEM lane r = key
@@ -62,19 +67,19 @@ constexpr int kQU = kDC * kQUCH;           // 32 KB
 constexpr int kVEC = 4 * kQT * 4;          // L (64), D (64), (alpha, E) (128) floats
 constexpr int kQUS = kQU + kVEC;           // one [Q | UQ] stage with its vectors
 constexpr int kDO = kDC * kQB;             // one dO stage: 16 KB
-constexpr int kNQ = 2, kND = 2;            // ring stages
+constexpr int kNQ = 3, kND = 1;            // ring stages
 constexpr int kRES_OFF = 0;                // K (2 chunks), UK (2 chunks)
 constexpr int kQU_OFF = kRES_OFF + 2 * kDC * kChunk;
 constexpr int kDO_OFF = kQU_OFF + kNQ * kQUS;
-constexpr int kOPS_OFF = kDO_OFF + kND * kDO;   // Gdp, dS, Gs tiles [128][64]
-constexpr int kREC_OFF = kOPS_OFF + 3 * kChunk; // per elementwise warp: 2 x 32 float2 query records
+constexpr int kOPS_OFF = kDO_OFF + kND * kDO;   // Gdp-then-dS, Gs tiles [128][64]
+constexpr int kREC_OFF = kOPS_OFF + 2 * kChunk; // per elementwise warp: 2 x 32 float2 query records
 constexpr int kSMEM = kREC_OFF + 8 * 64 * 8;
 static_assert(kQUS % 1024 == 0 && kQU_OFF % 1024 == 0 && kDO_OFF % 1024 == 0 && kOPS_OFF % 1024 == 0,
               "1024-byte aligned tiles");
 static_assert(kSMEM + 1024 <= 232448, "shared memory budget (1 KB static)");
 constexpr int kACC_K = 0, kACC_V = kD, kSC = 2 * kD, kTRES = kSC + 2 * kQT;   // TMEM columns
 static_assert(kTRES + 2 * (kD / 2) == 512, "TMEM budget");
-constexpr int kOP_GDP = 0, kOP_DS = 1, kOP_GS = 2;
+constexpr int kOP_GDP = 0, kOP_DS = 0, kOP_GS = 1;   // Gdp(t) and dS(t) share a tile
 
 struct ColParams {
   CUtensorMap mK, mUK;                       // resident, box {64, 128}
@@ -128,9 +133,13 @@ __device__ __forceinline__ bool ew_tile(const ColParams& p, ColCtrl& c, const Wa
   const float sc = p.tau * kLog2e;
   // The tile's per-query constants, formed once per warp instead of once per
   // (key, query): (-L log2e, alpha) for phase A and (D, alpha D - E) for
-  // phase B, in this warp's own records (a warp barrier orders them).
+  // phase B, in this warp's own records (a warp barrier orders them).  The
+  // loops read two queries' records with one broadcast 16-byte load: every
+  // shared-memory load costs the pipe a wavefront, however few bytes.
   float2* recA = rec;
   float2* recB = rec + 32;
+  const float4* recA4 = reinterpret_cast<const float4*>(recA);
+  const float4* recB4 = reinterpret_cast<const float4*>(recB);
   {
     const int lane = (int)(threadIdx.x & 31u), i = c0 + lane;
     const float Lq = vec[i], Dq = vec[kQT + i];
@@ -150,15 +159,18 @@ __device__ __forceinline__ bool ew_tile(const ColParams& p, ColCtrl& c, const Wa
     tc_fence_before();
     mbar_arrive(&c.s_empty[0]);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < 32; j += 2) {
+      const float4 v = recA4[j / 2];
       const int col = c0 + j;
-      const float2 v = recA[j];
       P[j] = (!MASK || (col >= lo && col <= hi)) ? ex2(fmaf(S[j], sc, v.x)) : 0.f;
+      P[j + 1] = (!MASK || (col + 1 >= lo && col + 1 <= hi)) ? ex2(fmaf(S[j + 1], sc, v.z)) : 0.f;
       bp[j] = fmaf(p.tau, B[j], -v.y);
+      bp[j + 1] = fmaf(p.tau, B[j + 1], -v.w);
     }
   }
-  // Gdp = P b' for gV; the previous tile's gV MMAs must have read the tile
-  if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(&c.gdp_empty, (t - 1) & 1, wt))) return false;
+  // Gdp = P b' for gV.  Its tile held dS(t-1): gK(t-1) must have read it
+  // (and Gs(t-1), which the same commit covers).
+  if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(&c.kop_empty, (t - 1) & 1, wt))) return false;
   {
     uint32_t w[16];
 #pragma unroll
@@ -174,17 +186,19 @@ __device__ __forceinline__ bool ew_tile(const ColParams& p, ColCtrl& c, const Wa
   tmem_ld16x4(sc_col, sc_col + 16, sc_col + 64, sc_col + 80, dP, dP + 16, C, C + 16);
   tc_fence_before();
   mbar_arrive(&c.s_empty[1]);
-  if (t > 0 && !__all_sync(0xffffffffu, mbar_wait(&c.kop_empty, (t - 1) & 1, wt))) return false;
+  // dS goes where Gdp(t) is: gV(t) must have read it
+  if (!__all_sync(0xffffffffu, mbar_wait(&c.gdp_empty, t & 1, wt))) return false;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {   // 16 columns at a time: dS and Gs for gK
     uint32_t wd[8], wg[8];
 #pragma unroll
     for (int j = 0; j < 16; j += 2) {
       float ds[2], gs[2];
+      const float4 v4 = recB4[(16 * h + j) / 2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int k = 16 * h + j + e;
-        const float2 v = recB[k];
+        const float2 v = e == 0 ? make_float2(v4.x, v4.y) : make_float2(v4.z, v4.w);
         const float te = dP[k] - v.x;
         ds[e] = P[k] * te;
         gs[e] = P[k] * (fmaf(bp[k], te, C[k]) + v.y);
