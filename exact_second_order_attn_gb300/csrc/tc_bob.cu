@@ -57,7 +57,7 @@ struct P1Params {
   CUtensorMap mK, mUK, mV, mUV;              // streamed, box {64, 32} (U1-and-Y sweep)
   CUtensorMap mK64, mV64;                    // streamed, box {64, 64} (Z sweep)
   CUtensorMap mUK64;                         // streamed, box {64, 64} (four-pass alpha sweep only)
-  CUtensorMap mdO_res;                       // resident, box {64, 128} (U1-and-Y sweep at d = 128)
+  CUtensorMap mdO_res, mUQ_res;              // resident, box {64, 128} (U1-and-Y sweeps, in shared memory)
   const __nv_bfloat16 *Q, *UQ, *dO;          // resident (copied into TMEM)
   const float *L, *D, *O;
   float *gQ, *gdO, *ws;
@@ -118,10 +118,14 @@ __device__ __forceinline__ void load_tile2(const CUtensorMap* m0, const CUtensor
 // writes the centred P o (B - alpha) (gdO = Y, nothing cancels).
 //
 // FULL (d = 64: the whole of pass 1 in one sweep): TMEM also holds the two
-// remaining alpha-free accumulators U2 += P K and W += dS K (four of 64
-// columns each, one score buffer of 128, Q, UQ, dO 96: 480 of 512), so the
-// row end applies the affine correction gQ = tau (U1 - EX U2 - alpha W)
-// directly and no Z sweep follows.
+// remaining alpha-free accumulators U2 += P K and W += dS K, so the row end
+// applies the affine correction gQ = tau (U1 - EX U2 - alpha W) directly and
+// no Z sweep follows.  The five operands go to TMEM as well (the accumulator
+// MMAs read only their B tiles from shared memory, and the elementwise warps
+// store no operand tiles there): TMEM = four accumulators of 64 columns, one
+// score buffer of 128, one operand buffer of 5 x 16 (shared by consecutive
+// tiles) and Q (32) = 496 of 512.  UQ and dO stay in shared memory as the A
+// operands of their score MMAs.
 template <int D_, bool DIRECT = false, bool FULL = false>
 struct PassU1Y {
   using Params = P1Params;
@@ -129,20 +133,21 @@ struct PassU1Y {
   static constexpr bool kWide = D == 128;
   static_assert(!FULL || (D == 64 && !DIRECT), "the one-sweep pass 1 fits TMEM at d = 64");
   static constexpr bool ROWS = true, SPLIT = kWide || FULL;
-  static constexpr int TRES = kWide ? 2 : 3;            // Q, UQ (, dO)
-  static constexpr int RES = kWide ? DC * kChunk : 0;   // dO in shared memory
+  static constexpr int TRES = FULL ? 1 : kWide ? 2 : 3;                      // Q (, UQ (, dO))
+  static constexpr int RES = FULL ? 2 * DC * kChunk : kWide ? DC * kChunk : 0;  // (UQ,) dO in shared memory
   static constexpr int ACH = 4 * kBlk;                  // [K | UK | V | UV] per 64-column chunk
   static constexpr int SA = DC * ACH, SA_TX = SA, SB = 0, SB_TX = 0;
   static constexpr bool kSplitPB = !DIRECT;             // PB as bf16 hi + lo (see above)
   static constexpr int NSA = kWide ? (kSplitPB ? 3 : 4) : 8, NSB = 0;
-  static constexpr bool VEC = false, ROW_SUMS = !DIRECT, TS = false;
+  static constexpr bool VEC = false, ROW_SUMS = !DIRECT, TS = FULL, ONE_OPS = FULL;
   static constexpr int VEC_OFF = 0, NVEC = 0, VEC_SCRATCH = 0;
   // dS, X, P, PB (, PB_lo) tiles; half h = columns 32h..32h+31
-  static constexpr int OPS = (kSplitPB ? 5 : 4) * kChunk;
+  static constexpr int OPS = FULL ? 0 : (kSplitPB ? 5 : 4) * kChunk;
+  static constexpr int TOPS = FULL ? 5 * (T / 2) : 0;   // TMEM operand columns (bf16 pairs)
   static constexpr int ACC = (FULL ? 4 : 2) * D;        // U1 | Y (| U2 | W)
   static constexpr int SCOLS = 128, NBUF = (kWide || FULL) ? 1 : 2;   // [S|B|dP|C]
   static constexpr int OP_HALF = 0, OP_COL = ACC + NBUF * SCOLS;
-  static constexpr int TRES_COL = OP_COL;
+  static constexpr int TRES_COL = OP_COL + TOPS;
   static constexpr int SMEM = RES + NSA * SA + OPS;
   // Ring-A order of the four 32-row blocks: [K | UK | V | UV], or with FULL
   // [V | UV | K | UK], where UV, K and K, UK are neighbours, so that two
@@ -159,6 +164,10 @@ struct PassU1Y {
     return s == 0 ? (const void*)p.Q : s == 1 ? (const void*)p.UQ : (const void*)p.dO;
   }
   __device__ static void load_res(const Params& p, uint8_t* res, uint64_t* bar, int row0, int head) {
+    if (FULL) {   // UQ then dO
+      for (int kc = 0; kc < DC; ++kc) tma_load_3d(res + kc * kChunk, &p.mUQ_res, bar, kc * 64, row0, head);
+      res += DC * kChunk;
+    }
     for (int kc = 0; kc < DC; ++kc) tma_load_3d(res + kc * kChunk, &p.mdO_res, bar, kc * 64, row0, head);
   }
   __device__ static void load_a(const Params& p, uint8_t* st, uint64_t* bar, int t, int head, bool) {
@@ -174,11 +183,17 @@ struct PassU1Y {
     for (int k = 0; k < D / 16; ++k)  // [S | Q UK^T] = Q [K; UK]^T
       mma_ts_w(sc, tres_a(tres, 0, D, k), kmaj(sa, ACH, BK * kBlk, k), i64, k > 0);
 #pragma unroll
-    for (int k = 0; k < D / 16; ++k)  // B += UQ K^T
-      mma_ts_w(sc + 32, tres_a(tres, 1, D, k), kmaj(sa, ACH, BK * kBlk, k), i32, 1);
+    for (int k = 0; k < D / 16; ++k) {  // B += UQ K^T
+      if (FULL)
+        mma_ss_w(sc + 32, res_lo(res, 0, DC, k), kmaj(sa, ACH, BK * kBlk, k), i32, 1);
+      else
+        mma_ts_w(sc + 32, tres_a(tres, 1, D, k), kmaj(sa, ACH, BK * kBlk, k), i32, 1);
+    }
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {  // [dP | C] = dO [V; UV]^T
-      if (kWide)
+      if (FULL)
+        mma_ss_w(sc + 64, res_lo(res, 1, DC, k), kmaj(sa, ACH, BV * kBlk, k), i64, k > 0);
+      else if (kWide)
         mma_ss_w(sc + 64, res_lo(res, 0, DC, k), kmaj(sa, ACH, BV * kBlk, k), i64, k > 0);
       else
         mma_ts_w(sc + 64, tres_a(tres, 2, D, k), kmaj(sa, ACH, BV * kBlk, k), i64, k > 0);
@@ -191,14 +206,16 @@ struct PassU1Y {
     for (int kk = 0; kk < T / 16; ++kk) {
       const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
       if constexpr (FULL) {
-        // N = 2d over two neighbouring 64-column blocks: LBO = one block
+        // N = 2d over two neighbouring 64-column blocks: LBO = one block;
+        // operand s of this tile at TMEM columns ops + 16 s, 16 keys per 8 columns
         const uint32_t amn2 = desc_lo(sa, kBlk);
         const uint32_t id2 = idesc_bf16(kM, 2 * D, false, true);
-        mma_ss_w(tb + A_Y, op_lo(ops, 2, h, kk), mnmaj(amn2, BUV * kBlk, kk), id2, acc0);  // [Y | U2] += P [UV | K]
-        mma_ss_w(tb + A_Y, op_lo(ops, 3, h, kk), mnmaj(amn, BV * kBlk, kk), id, 1);        // Y += PB V
-        mma_ss_w(tb + A_Y, op_lo(ops, 4, h, kk), mnmaj(amn, BV * kBlk, kk), id, 1);        // + PB_lo V
-        mma_ss_w(tb + A_W, op_lo(ops, 0, h, kk), mnmaj(amn2, BK * kBlk, kk), id2, acc0);   // [W | U1] += dS [K | UK]
-        mma_ss_w(tb + A_U1, op_lo(ops, 1, h, kk), mnmaj(amn, BK * kBlk, kk), id, 1);       // U1 += X K
+        const uint32_t a = ops + (uint32_t)(kk * 8);
+        mma_ts_w(tb + A_Y, a + 2 * 16, mnmaj(amn2, BUV * kBlk, kk), id2, acc0);  // [Y | U2] += P [UV | K]
+        mma_ts_w(tb + A_Y, a + 3 * 16, mnmaj(amn, BV * kBlk, kk), id, 1);        // Y += PB V
+        mma_ts_w(tb + A_Y, a + 4 * 16, mnmaj(amn, BV * kBlk, kk), id, 1);        // + PB_lo V
+        mma_ts_w(tb + A_W, a, mnmaj(amn2, BK * kBlk, kk), id2, acc0);            // [W | U1] += dS [K | UK]
+        mma_ts_w(tb + A_U1, a + 16, mnmaj(amn, BK * kBlk, kk), id, 1);           // U1 += X K
       } else {
         mma_ss_w(tb + A_U1, op_lo(ops, 0, h, kk), mnmaj(amn, BUK * kBlk, kk), id, acc0);   // U1 += dS UK
         mma_ss_w(tb + A_U1, op_lo(ops, 1, h, kk), mnmaj(amn, BK * kBlk, kk), id, 1);       // U1 += X K
@@ -275,12 +292,21 @@ struct PassU1Y {
         }
       }
       if (!kEarly && !s.acquire_ops()) return false;
-      const int col = 32 * (int)a.h + a.c0 + q * 16;
-      write_op_cols<8>(a.ops, (uint32_t)r, col, wdS);
-      write_op_cols<8>(a.ops + kChunk, (uint32_t)r, col, wX);
-      write_op_cols<8>(a.ops + 2 * kChunk, (uint32_t)r, col, wP);
-      write_op_cols<8>(a.ops + 3 * kChunk, (uint32_t)r, col, wPB);
-      if (kSplitPB) write_op_cols<8>(a.ops + 4 * kChunk, (uint32_t)r, col, wPBl);
+      if constexpr (FULL) {   // TMEM operands: 16 keys = 8 columns of each
+        const uint32_t o = a.ops + (uint32_t)((a.c0 + q * 16) / 2);
+        tmem_st8_nowait(o, wdS);
+        tmem_st8_nowait(o + 16, wX);
+        tmem_st8_nowait(o + 2 * 16, wP);
+        tmem_st8_nowait(o + 3 * 16, wPB);
+        tmem_st8_nowait(o + 4 * 16, wPBl);
+      } else {
+        const int col = 32 * (int)a.h + a.c0 + q * 16;
+        write_op_cols<8>(a.ops, (uint32_t)r, col, wdS);
+        write_op_cols<8>(a.ops + kChunk, (uint32_t)r, col, wX);
+        write_op_cols<8>(a.ops + 2 * kChunk, (uint32_t)r, col, wP);
+        write_op_cols<8>(a.ops + 3 * kChunk, (uint32_t)r, col, wPB);
+        if (kSplitPB) write_op_cols<8>(a.ops + 4 * kChunk, (uint32_t)r, col, wPBl);
+      }
     }
     s.publish_ops();
     return true;
@@ -824,7 +850,7 @@ bool make_p1(P1Params& p1, const BobArgs& a, const DevCtx& c, bool four_pass) {
   bool ok = make_bf16_map(&p1.mK, a.K, BH, N, a.d, kT) && make_bf16_map(&p1.mUK, a.UK, BH, N, a.d, kT) &&
             make_bf16_map(&p1.mV, a.V, BH, N, a.d, kT) && make_bf16_map(&p1.mUV, a.UV, BH, N, a.d, kT) &&
             make_bf16_map(&p1.mK64, a.K, BH, N, a.d, 64) && make_bf16_map(&p1.mV64, a.V, BH, N, a.d, 64) &&
-            make_bf16_map(&p1.mdO_res, a.dO, BH, N, a.d, kM);
+            make_bf16_map(&p1.mdO_res, a.dO, BH, N, a.d, kM) && make_bf16_map(&p1.mUQ_res, a.UQ, BH, N, a.d, kM);
   if (four_pass) ok = ok && make_bf16_map(&p1.mUK64, a.UK, BH, N, a.d, 64);
   if (!ok) return false;
   p1.Q = static_cast<const __nv_bfloat16*>(a.Q);

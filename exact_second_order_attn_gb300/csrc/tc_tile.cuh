@@ -43,6 +43,8 @@
 // device functions called below (see tc_bob.cu, tc_bwd.cu).
 #pragma once
 
+#include <type_traits>
+
 #include "tc_ptx.cuh"
 
 namespace fbob {
@@ -118,6 +120,7 @@ struct TileSync {
   int sa;         // ring-A stage of the tile
   bool vec;       // the tile's ring-A stage carries vectors read by the warpgroup
   bool ts;        // operands go to TMEM
+  bool one_ops;   // a single operand buffer (split columns): tile t reuses tile t-1's
 #ifdef FBOB_TRACE
   bool trace_on, trace_all;
   int t;
@@ -133,9 +136,14 @@ struct TileSync {
     mbar_arrive(&c->s_empty[q]);
   }
   // wait until the accumulator MMAs of this group's previous tile have read
-  // the operand half
+  // the operand half - with one operand buffer, those of the previous tile
   // (warp-uniform: the TMEM stores that follow are warp-collective)
   __device__ __forceinline__ bool acquire_ops() const {
+    if (one_ops) {
+      const int tp = 2 * k + q - 1;   // A(tp) completes phase tp >> 1 of o_empty[tp & 1]
+      if (tp < 0) return true;
+      return __all_sync(0xffffffffu, mbar_wait(&c->o_empty[tp & 1], (tp >> 1) & 1, *w));
+    }
     return __all_sync(0xffffffffu, mbar_wait(&c->o_empty[q], (k & 1) ^ 1, *w));
   }
   // operands written: hand them to the MMA thread (and release the ring-A
@@ -207,6 +215,13 @@ struct TileArgs {
 // beyond p.dv with zeros (the tensor maps carry the true width), the TMEM
 // residents are padded with zeros, so the score MMAs see zero-padded rows and
 // the accumulator columns >= p.dv stay zero and are never stored.
+// Op::ONE_OPS (optional, default false): one operand buffer shared by
+// consecutive tiles, for split columns where TMEM has no room for two.
+template <class Op, class = void>
+struct OneOps : std::false_type {};
+template <class Op>
+struct OneOps<Op, std::void_t<decltype(Op::ONE_OPS)>> : std::bool_constant<Op::ONE_OPS> {};
+
 template <class Op, bool CAUSAL, bool RAGGED>
 __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant__ typename Op::Params p) {
   static_assert(Op::NSB == 0 || Op::NSB == Op::NSA, "ring B stages pair with ring A stages");
@@ -214,6 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
   constexpr bool kSplit = Op::SPLIT;  // both warpgroups on every tile, half the columns each
   static_assert(!kSplit || Op::NBUF == 1, "split columns only with one score buffer");
   constexpr int kEwPerTile = kSplit ? 256 : 128;
+  constexpr bool kOneOps = OneOps<Op>::value;
+  static_assert(!kOneOps || (kSplit && Op::OP_HALF == 0), "one operand buffer: both warpgroups on every tile");
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ Ctrl ctrl;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -431,9 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1) tile_kernel(const __grid_constant
       FBOB_STAMP(2, t);
       tc_fence_after();
 #ifdef FBOB_TRACE
-      const TileSync sync{&ctrl, &wt, q, k, sa, Op::VEC, Op::TS, trace_on, trace_cta && ((warp & 1) == 1), t};
+      const TileSync sync{&ctrl, &wt, q, k, sa, Op::VEC, Op::TS, kOneOps, trace_on, trace_cta && ((warp & 1) == 1), t};
 #else
-      const TileSync sync{&ctrl, &wt, q, k, sa, Op::VEC, Op::TS};
+      const TileSync sync{&ctrl, &wt, q, k, sa, Op::VEC, Op::TS, kOneOps};
 #endif
       TileArgs ta;
       ta.sc = tb + lane + Op::ACC + (t % Op::NBUF) * Op::SCOLS;
