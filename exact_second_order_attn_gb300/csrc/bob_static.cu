@@ -70,6 +70,8 @@ const CtxFns& ctx_fns() {
   return fns;
 }
 
+}  // namespace
+
 // Process-unique id of the current context, or 0 if it cannot be read.
 unsigned long long current_ctx_id() {
   const CtxFns& f = ctx_fns();
@@ -80,8 +82,6 @@ unsigned long long current_ctx_id() {
   if (f.id(ctx, &id) != CUDA_SUCCESS) return 0;
   return id;
 }
-
-}  // namespace
 
 size_t static_workspace_rows() { return kStaticRows; }
 

@@ -65,5 +65,32 @@ cudaError_t tc_bob_cols_wide(const BobArgs& a, const DevCtx& c, cudaStream_t s);
 // bob_static.cu: the fixed (alpha, E) workspace of fbob_attn_bob_noalloc.
 size_t static_workspace_rows();           // capacity in query rows (B*H*N)
 cudaError_t static_workspace(float** ptr);  // device address on the current device
+unsigned long long current_ctx_id();       // process-unique id of the current context, 0 if unknown
+
+// side_stream.cu: a second stream of the current context for a launcher that
+// runs two independent halves of its work at the same time.  fork() makes the
+// side stream wait for the work queued so far on s; join() makes s wait for
+// everything queued on the side stream since.  The shared stream and events
+// are held (host lock) from fork() to join(), which the destructor runs if
+// the launcher did not.  Stream capture: both calls are capture-legal and the
+// side stream leaves the capture at join(); the first fork() in a context
+// creates the stream and events, so it should precede a capture.
+class SideStream {
+ public:
+  SideStream() = default;
+  SideStream(const SideStream&) = delete;
+  SideStream& operator=(const SideStream&) = delete;
+  ~SideStream();
+  cudaError_t fork(cudaStream_t s);
+  cudaError_t join();
+  cudaStream_t stream() const { return side_; }
+
+ private:
+  cudaStream_t origin_ = nullptr, side_ = nullptr;
+  void* slot_ = nullptr;   // the context's cached stream and events (locked while forked)
+};
+
+// Multiprocessors of the current device (0 if unknown).
+int sm_count();
 
 }  // namespace fbob

@@ -901,7 +901,7 @@ cudaError_t pass2_d(const BobArgs& a, const DevCtx& c, const dim3& grid, cudaStr
 }
 
 template <int D>
-cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
+cudaError_t bob_group(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   P1Params p1;
   if (!make_p1(p1, a, c, false)) return cudaErrorInvalidValue;
   const dim3 grid((a.N + kM - 1) / kM, a.BH);
@@ -916,6 +916,44 @@ cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if constexpr (D == 128) return tc_bob_cols_wide(a, c, s);
   else return pass2_d<D>(a, c, grid, s);
+}
+
+// Heads [h0, h0 + n) of a: every per-head array starts h0 heads further on.
+BobArgs head_range(const BobArgs& a, int h0, int n) {
+  const size_t nd = (size_t)a.N * a.d, n1 = (size_t)a.N;
+  auto bf = [&](const void* p) { return static_cast<const void*>(static_cast<const char*>(p) + 2 * h0 * nd); };
+  BobArgs b = a;
+  b.Q = bf(a.Q), b.K = bf(a.K), b.V = bf(a.V), b.dO = bf(a.dO), b.UQ = bf(a.UQ), b.UK = bf(a.UK), b.UV = bf(a.UV);
+  b.O = a.O + h0 * nd, b.L = a.L + h0 * n1, b.D = a.D + h0 * n1;
+  b.gQ = a.gQ + h0 * nd, b.gK = a.gK + h0 * nd, b.gV = a.gV + h0 * nd, b.gdO = a.gdO + h0 * nd;
+  b.ws = a.ws + 2 * h0 * n1;
+  b.BH = n;
+  return b;
+}
+
+// Whether to run the heads as two groups on two streams: when each pass's
+// launch is a few waves long and its last wave is mostly empty, one group's
+// pass 2 fills the SMs the other group's pass 1 tail leaves idle.  (One CTA
+// per SM at a time: every kernel here takes all 512 TMEM columns.)
+bool split_heads(const BobArgs& a) {
+  const int sms = sm_count();
+  if (a.BH < 2 || sms <= 0) return false;
+  const long ctas = (long)a.BH * ((a.N + kM - 1) / kM);
+  const long waves = (ctas + sms - 1) / sms;
+  const long idle = waves * sms - ctas;
+  return waves <= 16 && idle * 20 > waves * sms;   // more than 5 % of the slots idle
+}
+
+template <int D>
+cudaError_t bob_d(const BobArgs& a, const DevCtx& c, cudaStream_t s) {
+  if (!split_heads(a)) return bob_group<D>(a, c, s);
+  SideStream side;
+  if (side.fork(s) != cudaSuccess) return bob_group<D>(a, c, s);   // no side stream: run unsplit
+  const int h1 = a.BH / 2;
+  cudaError_t e0 = bob_group<D>(head_range(a, 0, h1), c, s);
+  cudaError_t e1 = bob_group<D>(head_range(a, h1, a.BH - h1), c, side.stream());
+  cudaError_t e2 = side.join();
+  return e0 != cudaSuccess ? e0 : e1 != cudaSuccess ? e1 : e2;
 }
 
 // The four-pass schedule: alpha sweep, E sweep, row-output sweep, column pass.
