@@ -21,8 +21,10 @@
  * Conventions shared by every call
  * --------------------------------
  * - All tensor arguments are DEVICE pointers owned by the caller.  The library
- *   never allocates, frees or synchronises inside these calls; every launch
- *   goes onto `stream` in order and the call returns before the GPU finishes.
+ *   never allocates device memory, frees or synchronises inside these calls;
+ *   every launch is ordered on `stream` (fbob_attn_bob may fork part of its
+ *   work onto a stream of its own and join it back, see there) and the call
+ *   returns before the GPU finishes.
  *   Outputs are overwritten, never accumulated into.
  * - Matrices are [B, H, N, d] row-major and contiguous (element (b, h, i, c)
  *   at ((b*H + h)*N + i)*d + c); row vectors (L, D) are [B, H, N]; the BoB
@@ -125,6 +127,15 @@ size_t fbob_bob_workspace_bytes(const fbob_problem* p);
  *   out: gQ, gK, gV, gdO [B,H,N,d] fp32;
  *        workspace [B,H,N,2] fp32 = (alpha_i, E_i) per row, at least
  *        fbob_bob_workspace_bytes(p) bytes (FBOB_ERR_WORKSPACE otherwise)
+ * Streams (bf16 inputs): when B*H >= 2 and each pass would end on a mostly
+ * empty wave of thread blocks, the heads run as two groups, the second on a
+ * library-owned stream forked from `stream` (it waits for the work already
+ * queued there) and joined back (`stream` waits for it before any later
+ * work).  Seen from `stream`, the call is ordered exactly as one launch
+ * sequence; results do not depend on the grouping.  The first such call in
+ * a CUDA context creates that stream and two events (kept until the process
+ * exits); make it before any stream capture, like the first
+ * fbob_attn_bob_noalloc call.
  */
 fbob_status fbob_attn_bob(const fbob_problem* p,
                           const void* Q, const void* K, const void* V,
