@@ -283,3 +283,33 @@ def test_head_groups_match_per_batch_calls(B, H, N, d, causal):
         for i, name in enumerate(("gQ", "gK", "gV", "gdO", "ws")):
             assert torch.equal(whole[i][b:b + 1], one[i]), (name, b)
     fb.device_status()
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", [(4, 3, 320, 64, False), (2, 3, 200, 128, True)])
+def test_bob_replays_in_a_cuda_graph(B, H, N, d, causal):
+    """fbob_attn_bob and fbob_attn_bob_noalloc captured in a CUDA graph (after a
+    first eager call in the context, as the header asks) replay to the eager
+    results bit for bit - including the two-stream head groups these shapes
+    take, whose fork and join must be capture-legal."""
+    w = attn_inputs.small(B, H, N, d, "bf16", seed=43)
+    x = {k: v.cuda() for k, v in attn_inputs.make_inputs(w).items()}
+    O, L = fb.attn_fwd(x["Q"], x["K"], x["V"], w.tau, causal=causal)
+    _, _, _, D = fb.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], L, w.tau, causal=causal)
+    args = (x["Q"], x["K"], x["V"], O, x["dO"], L, D, x["UQ"], x["UK"], x["UV"], w.tau)
+    outs = [torch.empty_like(O) for _ in range(4)] + [torch.empty(B, H, N, 2, device="cuda")]
+    nouts = [torch.empty_like(O) for _ in range(4)]
+    fb.fbob_attn_bob(*args, *outs, causal=causal)
+    fb.fbob_attn_bob_noalloc(*args, *nouts, causal=causal)
+    torch.cuda.synchronize()
+    ref, nref = [t.clone() for t in outs], [t.clone() for t in nouts]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fb.fbob_attn_bob(*args, *outs, causal=causal)
+        fb.fbob_attn_bob_noalloc(*args, *nouts, causal=causal)
+    for t in outs + nouts:
+        t.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    fb.device_status()
+    for a, b in zip(outs + nouts, ref + nref):
+        assert torch.equal(a, b)
