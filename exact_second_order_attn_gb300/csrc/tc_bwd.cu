@@ -332,7 +332,7 @@ auto pick(bool causal, bool ragged) {
 }
 
 template <int D>
-cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
+cudaError_t bwd_group(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
   DqParams q;
   if (!make_bf16_map(&q.mK, a.K, a.BH, a.N, a.d, DqOp<D>::T) || !make_bf16_map(&q.mV, a.V, a.BH, a.N, a.d, DqOp<D>::T))
     return cudaErrorInvalidValue;
@@ -370,6 +370,42 @@ cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
   k.wait_ns = c.wait_ns;
   k.stall = c.stall;
   return launch("attn_bwd_dkdv", pick<DkvOp<D>>(a.causal, ragged), DkvOp<D>::SMEM, tile::kThreads, grid, k, s);
+}
+
+// Heads [h0, h0 + n) of a: every per-head array starts h0 heads further on.
+BwdArgs head_range(const BwdArgs& a, int h0, int n) {
+  const size_t nd = (size_t)a.N * a.d, n1 = (size_t)a.N;
+  auto bf = [&](const void* p) { return static_cast<const void*>(static_cast<const char*>(p) + 2 * h0 * nd); };
+  BwdArgs b = a;
+  b.Q = bf(a.Q), b.K = bf(a.K), b.V = bf(a.V), b.dO = bf(a.dO);
+  b.O = a.O + h0 * nd, b.L = a.L + h0 * n1;
+  b.dQ = a.dQ + h0 * nd, b.dK = a.dK + h0 * nd, b.dV = a.dV + h0 * nd, b.D = a.D + h0 * n1;
+  b.BH = n;
+  return b;
+}
+
+// The dK/dV kernel reads the D the dq kernel writes, so the two run in stream
+// order.  When each launch would end on a mostly empty wave, the heads run as
+// two groups on two streams (as BoB does, tc_bob.cu) so that one group's dK/dV
+// kernel fills the SMs the other group's dq tail leaves idle.
+bool split_heads(const BwdArgs& a) {
+  const int sms = sm_count();
+  if (a.BH < 2 || sms <= 0) return false;
+  const long ctas = (long)a.BH * ((a.N + kM - 1) / kM);
+  const long waves = (ctas + sms - 1) / sms;
+  return waves <= 16 && (waves * sms - ctas) * 20 > waves * sms;
+}
+
+template <int D>
+cudaError_t bwd_d(const BwdArgs& a, const DevCtx& c, cudaStream_t s) {
+  if (!split_heads(a)) return bwd_group<D>(a, c, s);
+  SideStream side;
+  if (side.fork(s) != cudaSuccess) return bwd_group<D>(a, c, s);   // no side stream: run unsplit
+  const int h1 = a.BH / 2;
+  cudaError_t e0 = bwd_group<D>(head_range(a, 0, h1), c, s);
+  cudaError_t e1 = bwd_group<D>(head_range(a, h1, a.BH - h1), c, side.stream());
+  cudaError_t e2 = side.join();
+  return e0 != cudaSuccess ? e0 : e1 != cudaSuccess ? e1 : e2;
 }
 
 }  // namespace

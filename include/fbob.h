@@ -22,8 +22,9 @@
  * --------------------------------
  * - All tensor arguments are DEVICE pointers owned by the caller.  The library
  *   never allocates device memory, frees or synchronises inside these calls;
- *   every launch is ordered on `stream` (fbob_attn_bob may fork part of its
- *   work onto a stream of its own and join it back, see there) and the call
+ *   every launch is ordered on `stream` (fbob_attn_bwd and fbob_attn_bob may
+ *   fork part of their work onto a stream of their own and join it back, see
+ *   fbob_attn_bob) and the call
  *   returns before the GPU finishes.
  *   Outputs are overwritten, never accumulated into.
  * - Matrices are [B, H, N, d] row-major and contiguous (element (b, h, i, c)
@@ -100,6 +101,8 @@ fbob_status fbob_attn_fwd(const fbob_problem* p,
  *   in : Q, K, V, dO [B,H,N,d] dtype; O [B,H,N,d] fp32 and L [B,H,N] fp32
  *        from fbob_attn_fwd on the same Q, K, V
  *   out: dQ, dK, dV [B,H,N,d] fp32; D [B,H,N] fp32
+ * Streams: like fbob_attn_bob (bf16), the heads may run as two groups, the
+ * second on the library's forked stream; ordered on `stream` as one call.
  */
 fbob_status fbob_attn_bwd(const fbob_problem* p,
                           const void* Q, const void* K, const void* V,

@@ -267,10 +267,10 @@ def test_non_default_stream_and_repeatability():
 
 @pytest.mark.parametrize("B,H,N,d,causal", [(4, 3, 320, 64, False), (2, 3, 200, 128, True), (8, 12, 1024, 64, False)])
 def test_head_groups_match_per_batch_calls(B, H, N, d, causal):
-    """Every head's BoB depends on that head alone, so one call over B x H heads
-    (which the library may run as two head groups on two streams when a
-    launch's last wave would be mostly empty) must equal, bit for bit, one call
-    per batch entry (a different grouping, or none)."""
+    """Every head's first backward and BoB depend on that head alone, so one
+    call over B x H heads (which the library may run as two head groups on two
+    streams when a launch's last wave would be mostly empty) must equal, bit
+    for bit, one call per batch entry (a different grouping, or none)."""
     w = attn_inputs.small(B, H, N, d, "bf16", seed=31)
     x = {k: v.cuda() for k, v in attn_inputs.make_inputs(w).items()}
     O, L = fb.attn_fwd(x["Q"], x["K"], x["V"], w.tau, causal=causal)
@@ -278,10 +278,15 @@ def test_head_groups_match_per_batch_calls(B, H, N, d, causal):
     names = ("Q", "K", "V", "O", "dO", "L", "D", "UQ", "UK", "UV")
     full = dict(x, O=O, L=L, D=D)
     whole = fb.attn_bob(*(full[k] for k in names), w.tau, causal=causal)
+    whole_bwd = fb.attn_bwd(x["Q"], x["K"], x["V"], O, x["dO"], L, w.tau, causal=causal)
     for b in range(B):
         one = fb.attn_bob(*(full[k][b:b + 1].contiguous() for k in names), w.tau, causal=causal)
         for i, name in enumerate(("gQ", "gK", "gV", "gdO", "ws")):
             assert torch.equal(whole[i][b:b + 1], one[i]), (name, b)
+        sl = {k: full[k][b:b + 1].contiguous() for k in ("Q", "K", "V", "O", "dO", "L")}
+        one_bwd = fb.attn_bwd(sl["Q"], sl["K"], sl["V"], sl["O"], sl["dO"], sl["L"], w.tau, causal=causal)
+        for i, name in enumerate(("dQ", "dK", "dV", "D")):
+            assert torch.equal(whole_bwd[i][b:b + 1], one_bwd[i]), (name, b)
     fb.device_status()
 
 
