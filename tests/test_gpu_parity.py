@@ -318,3 +318,13 @@ def test_bob_replays_in_a_cuda_graph(B, H, N, d, causal):
     fb.device_status()
     for a, b in zip(outs + nouts, ref + nref):
         assert torch.equal(a, b)
+
+
+def test_wide_head_causal_sampled_heads():
+    """The causal bench configuration (B=2, H=16, N=16384, d=128, causal) at
+    full size, every output against the causal oracle on two sampled heads."""
+    w = attn_inputs.WORKLOADS["wide_head_b2h16_n16384_d128"]
+    heads = [(0, 3), (1, 12)]
+    gpu, inp = run_chain(w, causal=True)
+    ref = oracle_chain(oracle_inputs(inp, heads), w.tau, causal=True)
+    compare_all(select_heads(gpu, heads), ref, BF16_TOL, case="wide_head_b2h16_n16384_d128:causal")
